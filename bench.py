@@ -1,0 +1,425 @@
+"""Benchmark of the dual-mode attention forward pass on GB300.
+
+One step = one pass of the whole hot path (work-list build, the persistent
+tcgen05 attention kernel, the split-KV merge) over one batch.  Default
+workload: the batch-1 denoise loop (one 256-query bidirectional canvas over a
+32768-token cached context, Hq 32 / Hkv 4, head_dim 256); step s uses the
+canvas of denoise step s (fresh q and canvas K/V rows, drawn from seed 3+s),
+the cached context is reused, as in the loop the method runs.
+
+Timing: W untimed warm-up steps, then K steps.  Before every step (untimed)
+the step's canvas rows are written into the resident KV buffer and L2 is
+flushed by writing a 256 MiB buffer; each step is timed on its stream with CUDA
+events.  ``value`` is algorithmic TFLOP/s (4 * head_dim * Hq * visible pairs)
+summed over ranks.  ``e2e`` times the same steps through the public API with
+pinned host buffers: the step's canvas q/k/v go host -> device and out/lse come
+back device -> host inside the timed region.
+
+``--impl reference`` times the CPU fp64 oracle (the only reference this
+method has: there is no code to install) on a bounded sample of the same
+workload and prints the same line with ``"impl": "reference"``.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dual_mode_canvas_gb300 import binding  # noqa: E402
+from dual_mode_canvas_gb300 import replicas  # noqa: E402
+from dual_mode_canvas_gb300 import workloads as wls  # noqa: E402
+
+METRIC = "dual-mode attention TFLOP/s and denoise steps/s; % of tensor/HBM roofline"
+L2_FLUSH_BYTES = 256 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dram bytes per launch of the main kernel from the committed ncu capture (None until captured
+# for the current kernel)
+NCU_TRAFFIC_BYTES = {}
+
+
+def visible_pairs(wl) -> int:
+    """Visible (query, key) pairs of one query head: sum over rows of the
+    window size clipped to the sequence (causal: j <= i, bidirectional: all
+    keys; W narrows both)."""
+    tot = 0
+    W = wl.window
+    for c, n, md in wl.seqs:
+        L = c + n
+        i = c + np.arange(n, dtype=np.int64)
+        lo = np.zeros_like(i) if W < 0 else np.maximum(0, i - W)
+        if md == wls.CAUSAL:
+            hi = i
+        else:
+            hi = np.full_like(i, L - 1) if W < 0 else np.minimum(L - 1, i + W)
+        tot += int((hi - lo + 1).sum())
+    return tot
+
+
+def algorithmic_flops(wl) -> int:
+    return 4 * wl.head_dim * wl.num_q_heads * visible_pairs(wl)
+
+
+def algorithmic_bytes(wl) -> int:
+    """Q + out (bf16) + lse (fp32) + every K/V row some query sees, read once per KV head."""
+    W = wl.window
+    kv = 0
+    for c, n, md in wl.seqs:
+        L = c + n
+        lo = 0 if W < 0 else max(0, c - W)
+        hi = c + n - 1 if md == wls.CAUSAL else (L - 1 if W < 0 else min(L - 1, c + n - 1 + W))
+        kv += hi - lo + 1
+    q = wl.total_q * wl.num_q_heads * wl.head_dim * 2
+    return 2 * q + wl.total_q * wl.num_q_heads * 4 + 2 * kv * wl.num_kv_heads * wl.head_dim * 2
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    replicas.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    return replicas.aggregate(x, 0.0, device="cuda")[0]
+
+
+def run_gpu(args):
+    world, rank, local = dist_setup()
+    wl = wls.WORKLOADS[args.workload]
+    binding.load_library()
+    dev = torch.device("cuda")
+    batch = wls.make_batch(wl, device="cuda")
+    q, k, v = batch["q"], batch["k"], batch["v"]
+    cu_q, ctx, mode = batch["cu_q"].cuda(), batch["ctx_len"].cuda(), batch["mode"].cuda()
+    rows = wls.canvas_rows(wl)
+    nsteps = args.warmup + args.steps
+    loop = wl.steps > 1
+    # canvases of every step, drawn up front (device) and mirrored in pinned host memory
+    canv = []
+    if loop:
+        for s in range(nsteps):
+            step = s % wl.steps
+            if step == 0:
+                qs = q.clone()
+                kc = torch.cat([k[a:b] for a, b in rows])
+                vc = torch.cat([v[a:b] for a, b in rows])
+            else:
+                qs, kc, vc = wls.denoise_step_inputs(wl, step, device="cuda")
+            canv.append((qs, kc, vc))
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.total_q, wl.num_q_heads), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.workspace_size(len(wl.seqs), wl.total_q, wl.num_q_heads,
+                                            wl.num_kv_heads, wl.head_dim), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def stage(s):
+        if loop:
+            qs, kc, vc = canv[s]
+            q.copy_(qs)
+            o = 0
+            for a, b in rows:
+                k[a:b].copy_(kc[o:o + b - a])
+                v[a:b].copy_(vc[o:o + b - a])
+                o += b - a
+        flush.fill_(s & 0xFF)
+
+    flops = algorithmic_flops(wl)
+    nbytes = algorithmic_bytes(wl)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(nsteps)]
+    for e in ev:  # torch creates CUDA events lazily, on their first record
+        for x in e:
+            x.record(stream)
+    for s in range(args.warmup):
+        stage(s)
+        binding.forward(q, k, v, cu_q, ctx, mode, wl.window, wl.scale, out=out, lse=lse,
+                        workspace=ws)
+    torch.cuda.synchronize()
+    st = binding.status()
+    if st != binding.DG_OK:
+        raise RuntimeError(f"device status {st}: {binding.error_string(st)}")
+
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        for s in range(args.warmup, nsteps):
+            stage(s)
+            e0, e1, a0, a1 = ev[s]
+            e0.record(stream)
+            binding.forward(q, k, v, cu_q, ctx, mode, wl.window, wl.scale, out=out, lse=lse,
+                            workspace=ws, events=(a0, a1))
+            e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall0
+    st = binding.status()
+    if st != binding.DG_OK:
+        raise RuntimeError(f"device status {st}: {binding.error_string(st)}")
+    step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.warmup, nsteps)]
+    attn_ms = [ev[s][2].elapsed_time(ev[s][3]) for s in range(args.warmup, nsteps)]
+    tot_ms = max_over_ranks(world, float(sum(step_ms)))
+    ms_per_step = tot_ms / args.steps
+    attn_avg_ms = max_over_ranks(world, float(np.mean(attn_ms)))
+
+    # ---------------------------------------------- end to end, host buffers
+    e2e = None
+    if loop:
+        hq = [c[0].cpu().pin_memory() for c in canv]
+        hk = [c[1].cpu().pin_memory() for c in canv]
+        hv = [c[2].cpu().pin_memory() for c in canv]
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        kc_dev = torch.empty_like(canv[0][1])
+        vc_dev = torch.empty_like(canv[0][2])
+        e2e_ms = []
+        for s in range(nsteps):
+            flush.fill_(s & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            q.copy_(hq[s], non_blocking=True)
+            kc_dev.copy_(hk[s], non_blocking=True)
+            vc_dev.copy_(hv[s], non_blocking=True)
+            o = 0
+            for a, b in rows:
+                k[a:b].copy_(kc_dev[o:o + b - a])
+                v[a:b].copy_(vc_dev[o:o + b - a])
+                o += b - a
+            binding.forward(q, k, v, cu_q, ctx, mode, wl.window, wl.scale, out=out, lse=lse,
+                            workspace=ws)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if s >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+        e2e_tot = max_over_ranks(world, float(sum(e2e_ms)))
+        h2d = hq[0].numel() * 2 + hk[0].numel() * 2 + hv[0].numel() * 2
+        d2h = h_out.numel() * 2 + h_lse.numel() * 4
+        e2e = {"value": world * flops * args.steps / (e2e_tot * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_tot / args.steps}
+
+    if rank != 0:
+        return
+    peaks, peaks_src = load_peaks()
+    tflops = world * flops * args.steps / (tot_ms * 1e-3) / 1e12
+    attn_tflops = flops / (attn_avg_ms * 1e-3) / 1e12
+    sustained = args.steps * ms_per_step > 1000.0
+    tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    t_tc = flops / (tc_peak * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    if bound == "tensor":
+        roof = {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": round(attn_tflops / tc_peak, 4)}
+    else:
+        gbs = nbytes / (attn_avg_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    roof["traffic"] = NCU_TRAFFIC_BYTES.get(args.workload)
+    roof["peak_source"] = f"{peaks_src} ({'sustained' if (sustained and bound == 'tensor') else 'burst'})"
+    roof["kernel"] = "fwd_kernel (persistent tcgen05 attention)"
+    roof["kernel_ms_per_launch"] = round(attn_avg_ms, 4)
+    roof["tighter_roof_frac"] = round(max(t_tc, t_hbm) / (attn_avg_ms * 1e-3), 4)
+
+    res = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16)",
+        "config": {"workload": wl.name, "seqs_ctx_nq_mode": [list(s) for s in wl.seqs],
+                   "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
+                   "head_dim": wl.head_dim, "window": wl.window,
+                   "l2": "flushed before every step (256 MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "denoise_steps_per_s": round(1000.0 / ms_per_step, 2),
+        "algorithmic_gflop_per_step": round(flops / 1e9, 3),
+        "algorithmic_mb_per_step": round(nbytes / 1e6, 3),
+        "wall_s_timed_region": round(t_wall, 3),
+        "gpu_launches": 3 * args.steps * world,
+        "roofline": roof,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        res["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    print(json.dumps(res))
+
+
+def _oracle_sample(wl, q_heads):
+    """The bounded CPU sample: the first sequence's queries, ``q_heads`` query
+    heads of KV head 0, against its KV rows, through the fp64 oracle."""
+    import oracle
+    batch = wls.make_batch(wl, device="cpu") if wl.total_kv < (1 << 16) else None
+    if batch is None:
+        # build just the first sequence's rows on the host (same generator recipe)
+        b = wls.make_batch(wl, device="cuda")
+        c, n, md = wl.seqs[0]
+        qs = b["q"][:n, :q_heads].float().cpu().numpy().astype(np.float64)
+        ks = b["k"][:c + n, :1].float().cpu().numpy().astype(np.float64)
+        vs = b["v"][:c + n, :1].float().cpu().numpy().astype(np.float64)
+    else:
+        c, n, md = wl.seqs[0]
+        qs = batch["q"][:n, :q_heads].float().numpy().astype(np.float64)
+        ks = batch["k"][:c + n, :1].float().numpy().astype(np.float64)
+        vs = batch["v"][:c + n, :1].float().numpy().astype(np.float64)
+    one = wls.Workload("sample", (wl.seqs[0],), q_heads, 1, wl.head_dim, wl.window, wl.seed)
+    flops = algorithmic_flops(one)
+
+    def run():
+        oracle.attention(qs, ks, vs, [0, n], [c], [md], wl.window, wl.scale)
+    return run, flops
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    heads = max(1, wl.num_q_heads // wl.num_kv_heads)
+    run, flops = _oracle_sample(wl, heads)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        run()
+        reps += 1
+        if time.perf_counter() - t0 > budget_s or reps >= 50:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(flops * reps / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"fp64 NumPy oracle, first sequence of {wl.name}, {heads} query heads of KV head 0 "
+                      f"(of {wl.num_q_heads}), {reps} repetition(s) in {dt:.1f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = wls.WORKLOADS[args.workload]
+    run, flops = _oracle_sample(wl, 1)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    val = flops * args.steps / dt / 1e12
+    res = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16)",
+           "config": {"workload": wl.name, "sample": "first sequence, 1 query head"},
+           "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "kind": "oracle",
+                            "cores": len(os.sched_getaffinity(0)),
+                            "sample": f"fp64 NumPy oracle, first sequence of {wl.name}, query head 0 "
+                                      f"per step"},
+           "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="denoise_loop", choices=sorted(wls.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

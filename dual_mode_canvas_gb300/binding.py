@@ -1,0 +1,141 @@
+"""ctypes binding of the dg_attn C ABI (``include/dg_attn.h``).
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+library.  PyTorch supplies device memory and the current stream.  There is no
+fallback: if the library is missing or the GPU is not an sm_103 part, calls
+raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+DG_OK = 0
+DG_ERR_INVALID_ARG = 1
+DG_ERR_UNSUPPORTED = 2
+DG_ERR_CUDA = 3
+DG_ERR_WORKSPACE = 4
+DG_ERR_DEVICE_TIMEOUT = 5
+DG_ERR_DEVICE_BOUNDS = 6
+
+DG_MODE_CAUSAL = 0
+DG_MODE_BIDIRECTIONAL = 1
+
+EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profiled",
+            "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
+
+_lib = None
+
+
+class DgAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {error_string(code)} (status {code})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Loads ``lib/libdg_attn.so`` (built by ``build.build()``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"dg_attn CUDA library not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    lib.dg_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.dg_attn_workspace_size.restype = sz
+    lib.dg_attn_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                    ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.dg_attn_forward.restype = ctypes.c_int
+    lib.dg_attn_forward_profiled.argtypes = lib.dg_attn_forward.argtypes + [vp, vp]
+    lib.dg_attn_forward_profiled.restype = ctypes.c_int
+    lib.dg_attn_status.argtypes = [vp]
+    lib.dg_attn_status.restype = ctypes.c_int
+    lib.dg_attn_error_string.argtypes = [i32]
+    lib.dg_attn_error_string.restype = ctypes.c_char_p
+    lib.dg_attn_version.argtypes = []
+    lib.dg_attn_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def error_string(code: int) -> str:
+    return load_library().dg_attn_error_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(load_library().dg_attn_version())
+
+
+def workspace_size(num_seqs: int, total_q: int, num_q_heads: int, num_kv_heads: int,
+                   head_dim: int) -> int:
+    return int(load_library().dg_attn_workspace_size(num_seqs, total_q, num_q_heads, num_kv_heads,
+                                                     head_dim))
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def status(stream=None) -> int:
+    """Synchronises the stream and returns (then clears) the device status word."""
+    return int(load_library().dg_attn_status(_stream_handle(stream)))
+
+
+def forward(q, k, v, cu_q, ctx_len, mode, window: int, scale: float, *, out=None, lse=None,
+            workspace=None, stream=None, return_lse: bool = True, events=None):
+    """Dual-mode attention forward through ``dg_attn_forward``.
+
+    q [total_q, Hq, D] bf16, k/v [total_kv, Hkv, D] bf16, cu_q [B+1] int32,
+    ctx_len [B] int32, mode [B] uint8 (0 causal, 1 bidirectional), all on the
+    same CUDA device.  Returns ``(out, lse)`` (``lse`` None unless requested).
+    ``events=(begin, end)`` (torch.cuda.Event) goes through
+    ``dg_attn_forward_profiled``: the events bracket the main attention kernel.
+    """
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("cu_q", cu_q, torch.int32), ("ctx_len", ctx_len, torch.int32),
+                        ("mode", mode, torch.uint8)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    total_q, Hq, D = q.shape
+    total_kv, Hkv, Dk = k.shape
+    if tuple(v.shape) != (total_kv, Hkv, Dk) or Dk != D:
+        raise ValueError("k and v must both be [total_kv, Hkv, D]")
+    B = ctx_len.numel()
+    if cu_q.numel() != B + 1 or mode.numel() != B:
+        raise ValueError("cu_q must have num_seqs+1 entries and mode num_seqs")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    need = lib.dg_attn_workspace_size(B, total_q, Hq, Hkv, D)
+    if need == 0:
+        raise DgAttnError(DG_ERR_INVALID_ARG, "dg_attn_workspace_size")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(ctx_len), _ptr(mode), B, total_q, total_kv,
+            Hq, Hkv, D, int(window), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if events is None:
+        rc = lib.dg_attn_forward(*args)
+    else:
+        rc = lib.dg_attn_forward_profiled(*args, events[0].cuda_event, events[1].cuda_event)
+    if rc != DG_OK:
+        raise DgAttnError(rc, "dg_attn_forward")
+    return out, lse

@@ -1,0 +1,300 @@
+// Host side of the dg_attn C ABI (see include/dg_attn.h): argument checks,
+// TMA tensor maps, workspace layout, kernel launches and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "dg_attn.h"
+#include "kernels.cuh"
+
+namespace dg {
+
+__device__ int g_status;  // first device-side error since the last dg_attn_status()
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kVersion = 100;  // 0.1.0
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* status = nullptr;   // device address of g_status
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-head_dim kernel shapes: KV tile rows and pipeline stages.
+template <int D> struct Shape;
+template <> struct Shape<64> { static constexpr int BN = 128, NST = 3; };
+template <> struct Shape<128> { static constexpr int BN = 128, NST = 2; };
+template <> struct Shape<256> { static constexpr int BN = 64, NST = 2; };
+
+int kv_tile_rows(int D) {
+  return D == 64 ? Shape<64>::BN : D == 128 ? Shape<128>::BN : Shape<256>::BN;
+}
+
+template <int D>
+cudaError_t set_kernel_attrs() {
+  using S = Shape<D>;
+  using C = FwdCfg<D, S::BN, S::NST>;
+  return cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NST>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+}
+
+// One-time per-device setup (SM count, architecture, kernel attributes,
+// status word address).  Returns DG_OK or an error code.
+dg_status_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DG_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return DG_ERR_CUDA;
+    di.num_sms = prop.multiProcessorCount;
+    di.cc_major = prop.major;
+    di.cc_minor = prop.minor;
+    if (!(di.cc_major == 10 && di.cc_minor == 3)) return DG_ERR_UNSUPPORTED;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return DG_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (set_kernel_attrs<64>() != cudaSuccess || set_kernel_attrs<128>() != cudaSuccess ||
+        set_kernel_attrs<256>() != cudaSuccess)
+      return DG_ERR_CUDA;
+    void* sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_status) != cudaSuccess) return DG_ERR_CUDA;
+    di.status = static_cast<int*>(sym);
+    if (cudaMemset(di.status, 0, sizeof(int)) != cudaSuccess) return DG_ERR_CUDA;
+    di.ready = true;
+  }
+  *out = &di;
+  return DG_OK;
+}
+
+int num_ctas_for(const DeviceInfo& di) {
+  int n = di.num_sms;
+  if (const char* e = std::getenv("DG_ATTN_NUM_CTAS")) {
+    const int v = std::atoi(e);
+    if (v >= 1 && v < n) n = v;
+  }
+  return n;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  size_t hdr, seq_tile, seq_kv, tiles, unit_begin, part_lse, part_o, total;
+  int max_tiles;
+};
+
+Layout make_layout(int B, int total_q, int Hq, int Hkv, int D, int num_sms) {
+  const int G = Hq / Hkv;
+  const int TT = kRows / G;
+  Layout l;
+  const int64_t mt = (static_cast<int64_t>(total_q) + TT - 1) / TT + B;
+  l.max_tiles = static_cast<int>(static_cast<int64_t>(Hkv) * mt);
+  size_t off = 0;
+  l.hdr = off;        off = align256(off + sizeof(WorkHeader));
+  l.seq_tile = off;   off = align256(off + sizeof(int64_t) * (B + 1));
+  l.seq_kv = off;     off = align256(off + sizeof(int64_t) * (B + 1));
+  l.tiles = off;      off = align256(off + sizeof(TileDesc) * static_cast<size_t>(l.max_tiles));
+  l.unit_begin = off; off = align256(off + sizeof(int64_t) * (static_cast<size_t>(l.max_tiles) + 1));
+  l.part_lse = off;   off = align256(off + sizeof(float) * 2 * static_cast<size_t>(num_sms) * kRows);
+  l.part_o = off;     off = align256(off + sizeof(float) * 2 * static_cast<size_t>(num_sms) * kRows * D);
+  l.total = off;
+  return l;
+}
+
+bool sizes_ok(int B, int total_q, int Hq, int Hkv, int D) {
+  if (B < 0 || total_q < 0 || Hq <= 0 || Hkv <= 0) return false;
+  if (Hq % Hkv != 0 || Hq / Hkv > kRows) return false;
+  if (D != 64 && D != 128 && D != 256) return false;
+  return true;
+}
+
+// [rows, heads, D] bf16 tensor map, box {64, box_heads, box_rows}, 128-byte swizzle.
+dg_status_t encode_map(CUtensorMap* map, const void* base, int rows, int heads, int D,
+                       int box_heads, int box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(heads) * D * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_heads),
+                             static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DG_OK : DG_ERR_INVALID_ARG;
+}
+
+template <int D>
+dg_status_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                   const FwdParams& p, int num_ctas, int max_tiles, cudaStream_t stream,
+                   cudaEvent_t ev_begin, cudaEvent_t ev_end) {
+  using S = Shape<D>;
+  using C = FwdCfg<D, S::BN, S::NST>;
+  if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DG_ERR_CUDA;
+  fwd_kernel<D, S::BN, S::NST><<<num_ctas, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return DG_ERR_CUDA;
+  combine_kernel<D><<<max_tiles, 128, 0, stream>>>(p, num_ctas);
+  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  return DG_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" size_t dg_attn_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim) {
+  if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim)) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return make_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, sms).total;
+}
+
+namespace {
+dg_status_t forward_impl(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                         const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
+                         int32_t total_q, int32_t total_kv, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale,
+                         void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         void* stream_ptr, void* ev_begin, void* ev_end) {
+  if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim))
+    return (num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
+            num_q_heads / num_kv_heads > kRows) || (head_dim > 0 && head_dim != 64 &&
+            head_dim != 128 && head_dim != 256 && head_dim % 8 == 0)
+               ? DG_ERR_UNSUPPORTED
+               : DG_ERR_INVALID_ARG;
+  if (window < -1 || total_kv < 0 || !(scale > 0.f) || !std::isfinite(scale)) return DG_ERR_INVALID_ARG;
+  if (num_seqs == 0) return total_q == 0 ? DG_OK : DG_ERR_INVALID_ARG;
+  if (total_q == 0) return DG_OK;
+  if (total_kv < total_q) return DG_ERR_INVALID_ARG;
+  if (!q || !k || !v || !cu_q || !ctx_len || !mode || !out) return DG_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(cu_q, 4) || !aligned(ctx_len, 4) || (lse && !aligned(lse, 4)))
+    return DG_ERR_INVALID_ARG;
+
+  DeviceInfo* di = nullptr;
+  const dg_status_t st = device_info(&di);
+  if (st != DG_OK) return st;
+  const Layout lay = make_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, di->num_sms);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.total) return DG_ERR_WORKSPACE;
+
+  const int G = num_q_heads / num_kv_heads;
+  const int TT = kRows / G;
+  const int BN = kv_tile_rows(head_dim);
+  CUtensorMap mq, mk, mv;
+  if (encode_map(&mq, q, total_q, num_q_heads, head_dim, G, TT) != DG_OK ||
+      encode_map(&mk, k, total_kv, num_kv_heads, head_dim, 1, BN) != DG_OK ||
+      encode_map(&mv, v, total_kv, num_kv_heads, head_dim, 1, BN) != DG_OK)
+    return DG_ERR_INVALID_ARG;
+
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  FwdParams p;
+  p.ws.hdr = reinterpret_cast<WorkHeader*>(w + lay.hdr);
+  p.ws.seq_tile_off = reinterpret_cast<int64_t*>(w + lay.seq_tile);
+  p.ws.seq_kv_off = reinterpret_cast<int64_t*>(w + lay.seq_kv);
+  p.ws.tiles = reinterpret_cast<TileDesc*>(w + lay.tiles);
+  p.ws.unit_begin = reinterpret_cast<int64_t*>(w + lay.unit_begin);
+  p.ws.part_lse = reinterpret_cast<float*>(w + lay.part_lse);
+  p.ws.part_o = reinterpret_cast<float*>(w + lay.part_o);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = di->status;
+  p.Hq = num_q_heads;
+  p.G = G;
+  p.TT = TT;
+  p.window = window;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  build_worklist_kernel<<<1, 1024, 0, stream>>>(cu_q, ctx_len, mode, num_seqs, total_q, total_kv,
+                                                num_kv_heads, TT, BN, window, lay.max_tiles, p.ws,
+                                                p.status);
+  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  const int num_ctas = num_ctas_for(*di);
+  cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
+  switch (head_dim) {
+    case 64: return launch<64>(mq, mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
+    case 128: return launch<128>(mq, mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
+    default: return launch<256>(mq, mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
+  }
+}
+}  // namespace
+
+extern "C" dg_status_t dg_attn_forward(const void* q, const void* k, const void* v,
+                                       const int32_t* cu_q, const int32_t* ctx_len,
+                                       const uint8_t* mode, int32_t num_seqs, int32_t total_q,
+                                       int32_t total_kv, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t window, float scale, void* out,
+                                       float* lse, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
+                      num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
+                      stream, nullptr, nullptr);
+}
+
+extern "C" dg_status_t dg_attn_forward_profiled(
+    const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* ctx_len,
+    const uint8_t* mode, int32_t num_seqs, int32_t total_q, int32_t total_kv, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale, void* out, float* lse,
+    void* workspace, size_t workspace_bytes, void* stream, void* attn_begin_event,
+    void* attn_end_event) {
+  return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
+                      num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
+                      stream, attn_begin_event, attn_end_event);
+}
+
+extern "C" dg_status_t dg_attn_status(void* stream_ptr) {
+  DeviceInfo* di = nullptr;
+  const dg_status_t st = device_info(&di);
+  if (st != DG_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int h = 0;
+  if (cudaMemcpyAsync(&h, di->status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return DG_ERR_CUDA;
+  if (cudaMemsetAsync(di->status, 0, sizeof(int), stream) != cudaSuccess) return DG_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DG_ERR_CUDA;
+  return static_cast<dg_status_t>(h);
+}
+
+extern "C" const char* dg_attn_error_string(int32_t status) {
+  switch (status) {
+    case DG_OK: return "ok";
+    case DG_ERR_INVALID_ARG: return "invalid argument";
+    case DG_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case DG_ERR_CUDA: return "CUDA runtime error";
+    case DG_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DG_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
+    case DG_ERR_DEVICE_BOUNDS: return "a device-side bounds check failed";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int32_t dg_attn_version(void) { return kVersion; }
