@@ -33,11 +33,12 @@ std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// Per-head_dim kernel shapes: KV tile rows and pipeline stages.
+// Per-head_dim kernel shapes: KV tile rows, K-ring and V-ring stages (as many
+// as the 227 KB of shared memory holds next to Q and P).
 template <int D> struct Shape;
-template <> struct Shape<64> { static constexpr int BN = 128, NST = 3; };
-template <> struct Shape<128> { static constexpr int BN = 128, NST = 2; };
-template <> struct Shape<256> { static constexpr int BN = 64, NST = 2; };
+template <> struct Shape<64> { static constexpr int BN = 128, NK = 4, NV = 3; };
+template <> struct Shape<128> { static constexpr int BN = 128, NK = 3, NV = 2; };
+template <> struct Shape<256> { static constexpr int BN = 64, NK = 2, NV = 2; };
 
 int kv_tile_rows(int D) {
   return D == 64 ? Shape<64>::BN : D == 128 ? Shape<128>::BN : Shape<256>::BN;
@@ -46,8 +47,8 @@ int kv_tile_rows(int D) {
 template <int D>
 cudaError_t set_kernel_attrs() {
   using S = Shape<D>;
-  using C = FwdCfg<D, S::BN, S::NST>;
-  return cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NST>,
+  using C = FwdCfg<D, S::BN, S::NK, S::NV>;
+  return cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
 }
 
@@ -151,12 +152,13 @@ dg_status_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
                    const FwdParams& p, int num_ctas, int max_tiles, cudaStream_t stream,
                    cudaEvent_t ev_begin, cudaEvent_t ev_end) {
   using S = Shape<D>;
-  using C = FwdCfg<D, S::BN, S::NST>;
+  using C = FwdCfg<D, S::BN, S::NK, S::NV>;
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DG_ERR_CUDA;
-  fwd_kernel<D, S::BN, S::NST><<<num_ctas, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  fwd_kernel<D, S::BN, S::NK, S::NV><<<num_ctas, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return DG_ERR_CUDA;
-  combine_kernel<D><<<max_tiles, 128, 0, stream>>>(p, num_ctas);
+  const dim3 cgrid(max_tiles, (kRows + kCombineWarps - 1) / kCombineWarps);
+  combine_kernel<D><<<cgrid, kCombineWarps * 32, 0, stream>>>(p, num_ctas);
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   return DG_OK;
 }

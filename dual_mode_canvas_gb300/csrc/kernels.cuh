@@ -6,12 +6,13 @@
 //                          range is the union of the rows' windows (causal:
 //                          keys <= i, bidirectional: the whole sequence, both
 //                          narrowed to [i-W, i+W] on sliding-window layers).
-//   fwd_kernel<D,BN,NST>   persistent, one CTA per SM.  The (tile, KV-tile)
+//   fwd_kernel<D,BN,NK,NV> persistent, one CTA per SM.  The (tile, KV-tile)
 //                          work units are split evenly over the CTAs; a tile
 //                          cut between CTAs leaves fp32 partials + LSE.
-//                          Warp roles: warp 4 issues TMA loads, warp 5 issues
-//                          tcgen05 MMAs, warps 0-3 (one TMEM lane = one query
-//                          row each) run the online softmax and the epilogue.
+//                          Warp roles: warps 4 and 6 issue TMA loads (Q + K
+//                          ring, V ring), warp 5 issues tcgen05 MMAs, warps
+//                          0-3 (one TMEM lane = one query row each) run the
+//                          online softmax and the epilogue.
 //   combine_kernel<D>      merges the partials of cut tiles by their LSE.
 //
 // Rules (DiffusionGemma, agentlenshq page, "dual-mode operation", "dynamic
@@ -32,9 +33,10 @@
 namespace dg {
 
 constexpr int kRows = 128;          // query rows per tile (UMMA M, TMEM lanes)
-constexpr int kThreads = 192;       // 4 softmax warps + TMA warp + MMA warp
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 224;       // 4 softmax warps + Q/K loader + MMA issuer + V loader
+constexpr int kTmaWarp = 4;         // loads Q and the K ring
+constexpr int kMmaWarp = 5;         // issues tcgen05 MMAs, owns TMEM
+constexpr int kVLoadWarp = 6;       // loads the V ring
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitTimeoutNs = 250ull * 1000ull * 1000ull;
 
@@ -287,7 +289,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // -------------------------------------------------------------- main kernel
-template <int D, int BN, int NST>
+template <int D, int BN, int NK, int NV>
 struct FwdCfg {
   static constexpr int NKB = D / 64;                 // 128-byte column blocks of head_dim
   static constexpr int Q_BYTES = kRows * D * 2;
@@ -295,14 +297,15 @@ struct FwdCfg {
   static constexpr int P_BYTES = kRows * BN * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + NST * KV_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + NV * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
   // barriers
-  static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_KV_EMPTY = 2 + NST,
-                       B_S_FULL = 2 + 2 * NST, B_S_FREE = 4 + 2 * NST, B_P_FULL = 6 + 2 * NST,
-                       B_O_DONE = 7 + 2 * NST, B_O_FREE = 8 + 2 * NST, B_DRAIN = 9 + 2 * NST,
-                       NUM_BARS = 10 + 2 * NST;
+  static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = 2 + NK,
+                       B_V_FULL = 2 + 2 * NK, B_V_EMPTY = 2 + 2 * NK + NV,
+                       B_S_FULL = 2 + 2 * NK + 2 * NV, B_S_FREE = B_S_FULL + 2,
+                       B_P_FULL = B_S_FREE + 2, B_O_DONE = B_P_FULL + 1, B_O_FREE = B_O_DONE + 1,
+                       B_DRAIN = B_O_FREE + 1, NUM_BARS = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -314,11 +317,11 @@ struct FwdCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <int D, int BN, int NST>
+template <int D, int BN, int NK, int NV>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = FwdCfg<D, BN, NST>;
+  using C = FwdCfg<D, BN, NK, NV>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -349,9 +352,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_Q_FULL), 1);
     mbar_init(bar(C::B_Q_EMPTY), 1);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(bar(C::B_KV_FULL + s), 1);
-      mbar_init(bar(C::B_KV_EMPTY + s), 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(bar(C::B_K_FULL + s), 1);
+      mbar_init(bar(C::B_K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(bar(C::B_V_FULL + s), 1);
+      mbar_init(bar(C::B_V_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::B_S_FULL + b), 1);
@@ -382,50 +389,55 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   SegIter it{p.ws.unit_begin, num_tiles, u_beg, u_end, cta, true};
   const int G = p.G, TT = p.TT;
 
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ producer
+  if (warp == kTmaWarp || warp == kVLoadWarp) {
+    // ----------------------------------------------------------- producers
+    // warp 4 loads each segment's Q tile and the K ring, warp 6 the V ring,
+    // so a K tile is fetched as soon as its slot's QK^T has retired
     if (lane == 0) {
+      const bool is_k = (warp == kTmaWarp);
       const uint32_t q_tx = static_cast<uint32_t>(C::NKB * 64 * G * TT * 2);
-      const uint32_t kv_tx = static_cast<uint32_t>(2 * C::NKB * 64 * BN * 2);
+      const uint32_t t_tx = static_cast<uint32_t>(C::NKB * 64 * BN * 2);
+      const int NS = is_k ? NK : NV;
+      const uint32_t full0 = bar(is_k ? C::B_K_FULL : C::B_V_FULL);
+      const uint32_t empty0 = bar(is_k ? C::B_K_EMPTY : C::B_V_EMPTY);
+      const uint32_t ring = is_k ? sK : sV;
+      const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
       uint32_t stage = 0, phase = 0;
       int seg_i = 0;
       int q_issued_seg = -1;
-      int st_issued[NST];
-      uint32_t st_phase[NST];
-      for (int s = 0; s < NST; ++s) st_issued[s] = 0, st_phase[s] = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;  // per stage: a load was issued / its phase
       bool ok = true;
       Seg sg;
       while (ok && it.next(sg)) {
         const TileDesc td = p.ws.tiles[sg.tile];
-        if (!wait_phase(bar(C::B_Q_EMPTY), (seg_i & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(C::B_Q_FULL), q_tx);
+        if (is_k) {
+          if (!wait_phase(bar(C::B_Q_EMPTY), (seg_i & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(C::B_Q_FULL), q_tx);
 #pragma unroll
-        for (int kb = 0; kb < C::NKB; ++kb)
-          tma_load_3d(sQ + kb * (kRows * 128), &tm_q, bar(C::B_Q_FULL), kb * 64, td.kvh * G,
-                      td.q_row0);
-        q_issued_seg = seg_i;
+          for (int kb = 0; kb < C::NKB; ++kb)
+            tma_load_3d(sQ + kb * (kRows * 128), &tm_q, bar(C::B_Q_FULL), kb * 64, td.kvh * G,
+                        td.q_row0);
+          q_issued_seg = seg_i;
+        }
         for (int j = sg.j0; j < sg.j1; ++j) {
-          if (!wait_phase(bar(C::B_KV_EMPTY + stage), phase ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(C::B_KV_FULL + stage), kv_tx);
+          if (!wait_phase(empty0 + 8u * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(full0 + 8u * stage, t_tx);
           const int row = td.kv_row0 + (td.kt_first + j) * BN;
 #pragma unroll
-          for (int kb = 0; kb < C::NKB; ++kb) {
-            tma_load_3d(sK + stage * C::KV_BYTES + kb * (BN * 128), &tm_k, bar(C::B_KV_FULL + stage),
-                        kb * 64, td.kvh, row);
-            tma_load_3d(sV + stage * C::KV_BYTES + kb * (BN * 128), &tm_v, bar(C::B_KV_FULL + stage),
-                        kb * 64, td.kvh, row);
-          }
-          st_issued[stage] = 1;
-          st_phase[stage] = phase;
-          if (++stage == NST) { stage = 0; phase ^= 1; }
+          for (int kb = 0; kb < C::NKB; ++kb)
+            tma_load_3d(ring + stage * C::KV_BYTES + kb * (BN * 128), map, full0 + 8u * stage, kb * 64,
+                        td.kvh, row);
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == static_cast<uint32_t>(NS)) { stage = 0; phase ^= 1; }
         }
         ++seg_i;
       }
       if (!ok) {
         // let loads already in flight land before the CTA's shared memory goes away
         if (q_issued_seg >= 0) drain_wait(bar(C::B_Q_FULL), q_issued_seg & 1);
-        for (int s = 0; s < NST; ++s)
-          if (st_issued[s]) drain_wait(bar(C::B_KV_FULL + s), st_phase[s]);
+        for (int st = 0; st < NS; ++st)
+          if (issued_mask & (1u << st)) drain_wait(full0 + 8u * st, (issued_phase >> st) & 1);
       }
     }
     __syncwarp();
@@ -434,7 +446,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, BN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, D, 0, 1);
-      uint32_t qk_stage = 0, qk_phase = 0, pv_stage = 0, pv_phase = 0;
+      uint32_t k_stage = 0, k_phase = 0, v_stage = 0, v_phase = 0;
       uint32_t gj = 0;
       int seg_i = 0;
       bool ok = true;
@@ -447,14 +459,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           if (jj < n) {
             // S[g & 1] = Q K^T
             const uint32_t g = gj + jj;
-            if (!wait_phase(bar(C::B_KV_FULL + qk_stage), qk_phase, abort_flag, p.status) ||
+            if (!wait_phase(bar(C::B_K_FULL + k_stage), k_phase, abort_flag, p.status) ||
                 !wait_phase(bar(C::B_S_FREE + (g & 1)), ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t d_s = tmem + ((g & 1) ? C::TM_S1 : C::TM_S0);
-            const uint32_t k_base = sK + qk_stage * C::KV_BYTES;
+            const uint32_t k_base = sK + k_stage * C::KV_BYTES;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint64_t a = smem_desc_sw128(sQ + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024);
@@ -462,7 +474,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
               umma_bf16_ss(d_s, a, b, idesc_qk, kk > 0 ? 1u : 0u);
             }
             umma_commit(bar(C::B_S_FULL + (g & 1)));
-            if (++qk_stage == NST) { qk_stage = 0; qk_phase ^= 1; }
+            umma_commit(bar(C::B_K_EMPTY + k_stage));
+            if (++k_stage == NK) { k_stage = 0; k_phase ^= 1; }
           }
           if (jj >= 1) {
             // O (+)= P V
@@ -470,9 +483,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             const bool first = (jj == 1);
             if (first && seg_i > 0 &&
                 !wait_phase(bar(C::B_O_FREE), (seg_i - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-            if (!wait_phase(bar(C::B_P_FULL), g & 1, abort_flag, p.status)) { ok = false; break; }
+            if (!wait_phase(bar(C::B_P_FULL), g & 1, abort_flag, p.status) ||
+                !wait_phase(bar(C::B_V_FULL + v_stage), v_phase, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t v_base = sV + pv_stage * C::KV_BYTES;
+            const uint32_t v_base = sV + v_stage * C::KV_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
               const uint64_t a = smem_desc_sw128(sP + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024);
@@ -480,8 +494,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
               umma_bf16_ss(tmem + C::TM_O, a, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
             }
             umma_commit(bar(C::B_O_DONE));
-            umma_commit(bar(C::B_KV_EMPTY + pv_stage));
-            if (++pv_stage == NST) { pv_stage = 0; pv_phase ^= 1; }
+            umma_commit(bar(C::B_V_EMPTY + v_stage));
+            if (++v_stage == NV) { v_stage = 0; v_phase ^= 1; }
           }
         }
         if (!ok) break;
@@ -494,7 +508,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       drain_wait(bar(C::B_DRAIN), 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 4) {
     // -------------------------------------------- softmax + epilogue (rows)
     const int r = threadIdx.x;  // query row of the tile == TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
@@ -515,7 +529,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int i_lo = td.pos0, i_hi = td.pos0 + td.n_tok - 1;
       const int lo_all = W < 0 ? INT32_MIN / 2 : i_hi - W;  // largest row lower bound
       const int hi_all = min(td.L - 1, td.causal ? i_lo : (W < 0 ? td.L - 1 : i_lo + W));
-      float m_run = -INFINITY, l_run = 0.f;
+      // l_run: sum of the bf16 weights the PV MMA used (normalises O);
+      // l_lse: the same sum before rounding (gives the LSE)
+      float m_run = -INFINITY, l_run = 0.f, l_lse = 0.f;
       const int n = sg.j1 - sg.j0;
       for (int jj = 0; jj < n; ++jj) {
         const uint32_t g = gj + jj;
@@ -554,7 +570,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           rescale = true;
         }
         const float base = (m_use == -INFINITY) ? 0.f : m_use * sl2;
-        float rs = 0.f;
+        float rs = 0.f, rs_exact = 0.f;
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int c = 0; c < BN; c += 2) {
@@ -562,11 +578,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -base));
           const uint32_t w = pack_bf16x2(p0, p1);
           pk[c / 2] = w;
-          // the row sum uses the bf16 weights the PV MMA multiplies, so O / l
+          // normalise O by the bf16 weights the PV MMA multiplies, so O / l
           // stays a convex combination of the value rows
           rs += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+          rs_exact += p0 + p1;
         }
         l_run = l_run * alpha + rs;
+        l_lse = l_lse * alpha + rs_exact;
         m_run = m_use;
         if (jj > 0) {
           // PV of the previous tile has finished: P buffer free, O stable
@@ -599,7 +617,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (!__all_sync(0xffffffffu, wait_phase(bar(C::B_O_DONE), (gj + n - 1) & 1, abort_flag, p.status))) { ok = false; break; }
       tc_fence_after();
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      const float lse_v = l_run > 0.f ? m_run * p.scale + logf(l_run) : -INFINITY;
+      const float lse_v = l_lse > 0.f ? m_run * p.scale + logf(l_lse) : -INFINITY;
       if (sg.whole) {
         const int orow = td.q_row0 + t_row;
         const int h = td.kvh * G + g_row;
@@ -649,8 +667,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 }
 
 // ------------------------------------------------------------------ combine
+// One warp per (tile, row): the partial LSEs of the CTAs that shared the tile
+// are reduced across lanes, then every lane merges its columns.
+constexpr int kCombineWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const FwdParams p, int num_ctas) {
   const WorkHeader* hdr = p.ws.hdr;
   const int tile = blockIdx.x;
@@ -664,58 +686,60 @@ combine_kernel(const FwdParams p, int num_ctas) {
   const TileDesc td = p.ws.tiles[tile];
   const int G = p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.y * kCombineWarps + warp;
+  if (r >= G * p.TT) return;
+  const int t = r / G, gi = r - t * G;
+  if (t >= td.n_tok) return;
+  const int nc = c_hi - c_lo + 1;
+  auto slot_of = [&](int c) { return cta_unit_begin(c, U, P) >= T0 ? 2 * c : 2 * c + 1; };
+  float M = -INFINITY;
+  for (int i = lane; i < nc; i += 32)
+    M = fmaxf(M, p.ws.part_lse[static_cast<size_t>(slot_of(c_lo + i)) * kRows + r]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   constexpr int E = D / 32;  // columns per lane
-  for (int r = warp; r < G * p.TT; r += 4) {
-    const int t = r / G, gi = r - t * G;
-    if (t >= td.n_tok) continue;
-    float M = -INFINITY;
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const int slot = cta_unit_begin(c, U, P) >= T0 ? 2 * c : 2 * c + 1;
-      M = fmaxf(M, p.ws.part_lse[static_cast<size_t>(slot) * kRows + r]);
-    }
-    float acc[E];
+  float acc[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    float wsum = 0.f;
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const int slot = cta_unit_begin(c, U, P) >= T0 ? 2 * c : 2 * c + 1;
-      const float lk = p.ws.part_lse[static_cast<size_t>(slot) * kRows + r];
-      if (lk == -INFINITY) continue;
-      const float w = __expf(lk - M);
-      wsum += w;
-      const float* src = p.ws.part_o + (static_cast<size_t>(slot) * kRows + r) * D;
-      if constexpr (E % 4 == 0) {
-#pragma unroll
-        for (int k = 0; k < E / 4; ++k) {
-          const float4 x = *reinterpret_cast<const float4*>(src + (k * 32 + lane) * 4);
-          acc[4 * k + 0] += w * x.x;
-          acc[4 * k + 1] += w * x.y;
-          acc[4 * k + 2] += w * x.z;
-          acc[4 * k + 3] += w * x.w;
-        }
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src + lane * 2);
-        acc[0] += w * x.x;
-        acc[1] += w * x.y;
-      }
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int orow = td.q_row0 + t;
-    const int h = td.kvh * G + gi;
-    __nv_bfloat16* dst = p.out + (static_cast<size_t>(orow) * p.Hq + h) * D;
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  for (int i = 0; i < nc; ++i) {
+    const int slot = slot_of(c_lo + i);
+    const float lk = p.ws.part_lse[static_cast<size_t>(slot) * kRows + r];
+    if (lk == -INFINITY) continue;
+    const float w = __expf(lk - M);
+    wsum += w;
+    const float* src = p.ws.part_o + (static_cast<size_t>(slot) * kRows + r) * D;
     if constexpr (E % 4 == 0) {
 #pragma unroll
       for (int k = 0; k < E / 4; ++k) {
-        const uint32_t w0 = pack_bf16x2(acc[4 * k + 0] * inv, acc[4 * k + 1] * inv);
-        const uint32_t w1 = pack_bf16x2(acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
-        *reinterpret_cast<uint2*>(dst + (k * 32 + lane) * 4) = make_uint2(w0, w1);
+        const float4 x = *reinterpret_cast<const float4*>(src + (k * 32 + lane) * 4);
+        acc[4 * k + 0] += w * x.x;
+        acc[4 * k + 1] += w * x.y;
+        acc[4 * k + 2] += w * x.z;
+        acc[4 * k + 3] += w * x.w;
       }
     } else {
-      *reinterpret_cast<uint32_t*>(dst + lane * 2) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      const float2 x = *reinterpret_cast<const float2*>(src + lane * 2);
+      acc[0] += w * x.x;
+      acc[1] += w * x.y;
     }
-    if (lane == 0 && p.lse != nullptr)
-      p.lse[static_cast<size_t>(orow) * p.Hq + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
   }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int orow = td.q_row0 + t;
+  const int h = td.kvh * G + gi;
+  __nv_bfloat16* dst = p.out + (static_cast<size_t>(orow) * p.Hq + h) * D;
+  if constexpr (E % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k) {
+      const uint32_t w0 = pack_bf16x2(acc[4 * k + 0] * inv, acc[4 * k + 1] * inv);
+      const uint32_t w1 = pack_bf16x2(acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
+      *reinterpret_cast<uint2*>(dst + (k * 32 + lane) * 4) = make_uint2(w0, w1);
+    }
+  } else {
+    *reinterpret_cast<uint32_t*>(dst + lane * 2) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[static_cast<size_t>(orow) * p.Hq + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
 }  // namespace dg

@@ -56,23 +56,32 @@ def f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def check(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
+# Rows whose softmax mass sits on a handful of keys (windows of 0-1, the first
+# rows of a prefill) have |out| up to ~4.  There the bf16 output rounding alone
+# is up to 2^-8 |out| and the bf16 weights the PV MMA multiplies add up to 2^-8
+# of the value spread, so the edge-case tests allow 1e-2 + 2^-7 |ref| per
+# element; every configured workload is held to the plain 1e-2.
+EDGE_REL = 2.0 ** -7
+
+
+def check(out_gpu, lse_gpu, out_ref, lse_ref, what="", rel=0.0):
     d = np.abs(out_gpu - out_ref)
     dl = np.abs(lse_gpu - lse_ref)
     assert np.isfinite(out_gpu).all() and np.isfinite(lse_gpu).all(), what
-    assert d.max() <= MAX_ABS, f"{what} max|dout|={d.max():.3g}"
+    excess = d - (MAX_ABS + rel * np.abs(out_ref))
+    assert excess.max() <= 0, f"{what} max|dout|={d.max():.3g} (worst excess {excess.max():.3g})"
     assert d.mean() <= MEAN_ABS, f"{what} mean|dout|={d.mean():.3g}"
     assert dl.max() <= LSE_ABS, f"{what} max|dlse|={dl.max():.3g}"
 
 
-def full_check(wl, batch, window=None, dev=None):
+def full_check(wl, batch, window=None, dev=None, rel=0.0):
     window = wl.window if window is None else window
     dev = to_dev(batch) if dev is None else dev
     out, lse = run_gpu(dev, window, wl.scale)
     ref_o, ref_l = oracle.attention(f64(batch["q"]), f64(batch["k"]), f64(batch["v"]),
                                     batch["cu_q"].numpy(), batch["ctx_len"].numpy(),
                                     batch["mode"].numpy(), window, wl.scale)
-    check(f64(out), f64(lse), ref_o, ref_l, wl.name)
+    check(f64(out), f64(lse), ref_o, ref_l, f"{wl.name} W={window}", rel=rel)
     return out, lse
 
 
@@ -106,7 +115,7 @@ def test_ragged_edge_cases(case):
     wl, batch = wls.random_batch(100 + case, seqs, Hq, Hkv, D, -1)
     dev = to_dev(batch)
     for W in windows:
-        full_check(wl, batch, window=W, dev=dev)
+        full_check(wl, batch, window=W, dev=dev, rel=EDGE_REL)
 
 
 def test_single_visible_key_is_exact():
