@@ -27,7 +27,7 @@ DG_MODE_CAUSAL = 0
 DG_MODE_BIDIRECTIONAL = 1
 
 EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profiled",
-            "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
+            "dg_attn_forward_noalloc", "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
 
 _lib = None
 
@@ -59,6 +59,9 @@ def load_library():
     lib.dg_attn_forward.restype = ctypes.c_int
     lib.dg_attn_forward_profiled.argtypes = lib.dg_attn_forward.argtypes + [vp, vp]
     lib.dg_attn_forward_profiled.restype = ctypes.c_int
+    lib.dg_attn_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                            i32, ctypes.c_float, vp, vp, vp]
+    lib.dg_attn_forward_noalloc.restype = ctypes.c_int
     lib.dg_attn_status.argtypes = [vp]
     lib.dg_attn_status.restype = ctypes.c_int
     lib.dg_attn_error_string.argtypes = [i32]

@@ -17,6 +17,11 @@ namespace dg {
 
 __device__ int g_status;  // first device-side error since the last dg_attn_status()
 
+// Scratch of dg_attn_forward_noalloc.  Host code must not use this name as an
+// address: it reaches the kernels only through the device address looked up
+// once per device (DeviceInfo::noalloc_scratch).
+static __device__ __align__(256) uint8_t g_noalloc_scratch[DG_ATTN_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -27,6 +32,7 @@ struct DeviceInfo {
   int num_sms = 0;
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;   // device address of g_status
+  void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
 };
 
 std::mutex g_mutex;
@@ -82,6 +88,10 @@ dg_status_t device_info(DeviceInfo** out) {
     void* sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status) != cudaSuccess) return DG_ERR_CUDA;
     di.status = static_cast<int*>(sym);
+    void* scratch = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr)
+      return DG_ERR_CUDA;
+    di.noalloc_scratch = scratch;
     if (cudaMemset(di.status, 0, sizeof(int)) != cudaSuccess) return DG_ERR_CUDA;
     di.ready = true;
   }
@@ -271,6 +281,30 @@ extern "C" dg_status_t dg_attn_forward_profiled(
   return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
                       num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
                       stream, attn_begin_event, attn_end_event);
+}
+
+// For callers that cannot allocate device memory (see the header): the same
+// forward pass, with the workspace taken from the library's static scratch.
+extern "C" dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, const void* v,
+                                               const int32_t* cu_q, const int32_t* ctx_len,
+                                               const uint8_t* mode, int32_t num_seqs,
+                                               int32_t total_q, int32_t total_kv,
+                                               int32_t num_q_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t window, float scale,
+                                               void* out, float* lse, void* stream) {
+  if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim) || num_seqs == 0 ||
+      total_q == 0)
+    return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
+                        num_kv_heads, head_dim, window, scale, out, lse, nullptr, 0, stream,
+                        nullptr, nullptr);
+  DeviceInfo* di = nullptr;
+  const dg_status_t st = device_info(&di);
+  if (st != DG_OK) return st;
+  const Layout lay = make_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, di->num_sms);
+  if (lay.total > DG_ATTN_NOALLOC_SCRATCH_BYTES) return DG_ERR_WORKSPACE;
+  return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
+                      num_kv_heads, head_dim, window, scale, out, lse, di->noalloc_scratch,
+                      DG_ATTN_NOALLOC_SCRATCH_BYTES, stream, nullptr, nullptr);
 }
 
 extern "C" dg_status_t dg_attn_status(void* stream_ptr) {

@@ -109,6 +109,39 @@ dg_status_t dg_attn_forward_profiled(const void* q, const void* k, const void* v
                                      void* workspace, size_t workspace_bytes,
                                      void* stream, void* attn_begin_event, void* attn_end_event);
 
+/* Capacity, in bytes, of the static scratch array used by
+ * dg_attn_forward_noalloc (48 MiB). */
+#define DG_ATTN_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
+
+/* The forward pass for callers that cannot allocate device memory: callers
+ * embedded in a host framework that owns every device allocation (a
+ * pre-planned arena, a plugin interface that hands out no scratch), or loops
+ * that cannot afford cudaMalloc's device-wide synchronisation between steps.
+ * The pages describe no such entry point; it exists for those callers only.
+ *
+ * Same arguments and results as dg_attn_forward without the workspace: the
+ * scratch is a file-scope __device__ array of DG_ATTN_NOALLOC_SCRATCH_BYTES
+ * inside this library, which every GPU that loads the library holds until the
+ * process exits.  The caller still owns q, k, v, the metadata, out and lse.
+ *
+ *   - Returns DG_ERR_WORKSPACE, having enqueued nothing, when these sizes
+ *     need more scratch than the array holds (dg_attn_workspace_size() tells
+ *     the requirement).
+ *   - Calls no cudaMalloc / cudaFree and no allocating library routine.
+ *   - Every call on a device shares the one array, and it keeps the last
+ *     call's contents; nothing in it needs to start at zero.  Calls whose
+ *     work overlaps on the GPU (other streams, other threads) race on it:
+ *     serialise them.
+ *   - The first call of any dg_attn entry point on a device looks up the
+ *     array's device address (a one-time set-up per device); make that
+ *     first call before any stream capture. */
+dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, const void* v,
+                                    const int32_t* cu_q, const int32_t* ctx_len,
+                                    const uint8_t* mode, int32_t num_seqs, int32_t total_q,
+                                    int32_t total_kv, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t window, float scale,
+                                    void* out, float* lse, void* stream);
+
 /* Synchronises `stream`, returns the current device's status word (DG_OK if
  * no device-side error was recorded since the last call) and clears it. */
 dg_status_t dg_attn_status(void* stream);
