@@ -92,56 +92,102 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """SM clock and clock-event-reason sampling during the timed region.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Polls NVML (read-only queries through ctypes) from a background thread
+    every ~0.5 ms, so even a few-millisecond timed region is covered; falls
+    back to ``nvidia-smi -lms 100`` when NVML cannot be loaded."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, device_index: int):
         self.dev = device_index
-        self.proc = None
+        self.samples = []
+        self.max_mhz = None
+        self._stop = False
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        self.source = "none"
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        handle = ctypes.c_void_p()
+        try:
+            bus = torch.cuda.get_device_properties(self.dev)
+            busid = f"{bus.pci_domain_id:08x}:{bus.pci_bus_id:02x}:{bus.pci_device_id:02x}.0".encode()
+            rc = lib.nvmlDeviceGetHandleByPciBusId_v2(busid, ctypes.byref(handle))
+        except AttributeError:
+            rc = 1
+        if rc != 0 and lib.nvmlDeviceGetHandleByIndex_v2(self.dev, ctypes.byref(handle)) != 0:
+            return False
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self._nvml, self._handle = lib, handle
+        return True
+
+    def _poll(self):
+        import ctypes
+        mhz, reasons = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(self._nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop:
+            if self._nvml.nvmlDeviceGetClockInfo(self._handle, 1, ctypes.byref(mhz)) == 0:
+                rs = reasons.value if get_reasons(self._handle, ctypes.byref(reasons)) == 0 else 0
+                self.samples.append((float(mhz.value), int(rs)))
+            time.sleep(0.0005)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+        import threading
+        if self._open_nvml():
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            t0 = time.perf_counter()
+            while not self.samples and time.perf_counter() - t0 < 1.0:
+                time.sleep(0.001)
+        else:
+            self.source = "nvidia-smi"
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=clocks.sm,clocks.max.sm",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        if self._thread is not None:
+            self._stop = True
+            self._thread.join(timeout=5)
+        elif self.source == "nvidia-smi":
+            self._proc.terminate()
+            out, _ = self._proc.communicate(timeout=10)
+            for ln in out.splitlines():
+                parts = [x.strip() for x in ln.split(",")]
+                try:
+                    self.samples.append((float(parts[0]), 0))
+                    self.max_mhz = float(parts[1])
+                except (ValueError, IndexError):
+                    pass
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for nm, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "samples": 0, "source": self.source}
+        reasons = set()
+        for _, rs in self.samples:
+            for bit, name in self.REASONS.items():
+                if rs & bit:
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([m for m, _ in self.samples])), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples), "source": self.source}
 
 
 def dist_setup():

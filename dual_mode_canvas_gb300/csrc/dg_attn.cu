@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -27,9 +28,15 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kVersion = 100;  // 0.1.0
 
+constexpr int kClusterSizes[] = {1, 2, 4, 8};
+
+int cluster_slot(int C) { return C == 1 ? 0 : C == 2 ? 1 : C == 4 ? 2 : 3; }
+int dim_slot(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
+
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
+  int max_clusters[3][4] = {};  // [head_dim][cluster size]: co-resident clusters
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;   // device address of g_status
   void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
@@ -39,23 +46,45 @@ std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// Per-head_dim kernel shapes: KV tile rows, K-ring and V-ring stages (as many
-// as the 227 KB of shared memory holds next to Q and P).
+// Per-head_dim kernel shapes: KV tile rows (TMEM holds O, two S/P buffers of
+// BN columns and Q) and K-ring / V-ring stages (shared memory holds only the
+// rings, up to 224 KB).
 template <int D> struct Shape;
-template <> struct Shape<64> { static constexpr int BN = 128, NK = 4, NV = 3; };
-template <> struct Shape<128> { static constexpr int BN = 128, NK = 3, NV = 2; };
-template <> struct Shape<256> { static constexpr int BN = 64, NK = 2, NV = 2; };
+template <> struct Shape<64> { static constexpr int BN = 128, NK = 6, NV = 6; };
+template <> struct Shape<128> { static constexpr int BN = 128, NK = 4, NV = 3; };
+template <> struct Shape<256> { static constexpr int BN = 64, NK = 4, NV = 3; };
 
 int kv_tile_rows(int D) {
   return D == 64 ? Shape<64>::BN : D == 128 ? Shape<128>::BN : Shape<256>::BN;
 }
 
 template <int D>
-cudaError_t set_kernel_attrs() {
+cudaError_t set_kernel_attrs(DeviceInfo& di) {
   using S = Shape<D>;
   using C = FwdCfg<D, S::BN, S::NK, S::NV>;
-  return cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  // how many clusters of each size fit on the device at once (persistent grid)
+  for (int cs : kClusterSizes) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs * (di.num_sms / cs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel<D, S::BN, S::NK, S::NV>, &cfg) != cudaSuccess)
+      n = 0;
+    di.max_clusters[dim_slot(D)][cluster_slot(cs)] = n;
+  }
+  cudaGetLastError();
+  return cudaSuccess;
 }
 
 // One-time per-device setup (SM count, architecture, kernel attributes,
@@ -82,8 +111,8 @@ dg_status_t device_info(DeviceInfo** out) {
         return DG_ERR_CUDA;
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    if (set_kernel_attrs<64>() != cudaSuccess || set_kernel_attrs<128>() != cudaSuccess ||
-        set_kernel_attrs<256>() != cudaSuccess)
+    if (set_kernel_attrs<64>(di) != cudaSuccess || set_kernel_attrs<128>(di) != cudaSuccess ||
+        set_kernel_attrs<256>(di) != cudaSuccess)
       return DG_ERR_CUDA;
     void* sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status) != cudaSuccess) return DG_ERR_CUDA;
@@ -99,11 +128,26 @@ dg_status_t device_info(DeviceInfo** out) {
   return DG_OK;
 }
 
-int num_ctas_for(const DeviceInfo& di) {
-  int n = di.num_sms;
-  if (const char* e = std::getenv("DG_ATTN_NUM_CTAS")) {
+// Cluster size for a call: C query tiles of one (sequence, KV head) share
+// every K/V load.  DG_ATTN_CLUSTER (1, 2, 4 or 8) overrides the default.
+int cluster_for(const DeviceInfo& di, int D) {
+  int C = 2;
+  if (const char* e = std::getenv("DG_ATTN_CLUSTER")) {
     const int v = std::atoi(e);
-    if (v >= 1 && v < n) n = v;
+    if (v == 1 || v == 2 || v == 4 || v == 8) C = v;
+  }
+  while (C > 1 && di.max_clusters[dim_slot(D)][cluster_slot(C)] < 1) C >>= 1;
+  return C;
+}
+
+// Persistent grid: as many clusters as are co-resident (DG_ATTN_NUM_CTAS caps
+// the number of CTAs, for tests of the split-KV path).
+int num_clusters_for(const DeviceInfo& di, int D, int C) {
+  int n = C == 1 ? di.num_sms : di.max_clusters[dim_slot(D)][cluster_slot(C)];
+  if (n < 1) n = 1;
+  if (const char* e = std::getenv("DG_ATTN_NUM_CTAS")) {
+    const int v = std::max(1, std::atoi(e) / C);
+    if (v < n) n = v;
   }
   return n;
 }
@@ -125,7 +169,7 @@ Layout make_layout(int B, int total_q, int Hq, int Hkv, int D, int num_sms) {
   l.hdr = off;        off = align256(off + sizeof(WorkHeader));
   l.seq_tile = off;   off = align256(off + sizeof(int64_t) * (B + 1));
   l.seq_kv = off;     off = align256(off + sizeof(int64_t) * (B + 1));
-  l.tiles = off;      off = align256(off + sizeof(TileDesc) * static_cast<size_t>(l.max_tiles));
+  l.tiles = off;      off = align256(off + sizeof(TileDesc) * kMaxCluster * static_cast<size_t>(l.max_tiles));
   l.unit_begin = off; off = align256(off + sizeof(int64_t) * (static_cast<size_t>(l.max_tiles) + 1));
   l.part_lse = off;   off = align256(off + sizeof(float) * 2 * static_cast<size_t>(num_sms) * kRows);
   l.part_o = off;     off = align256(off + sizeof(float) * 2 * static_cast<size_t>(num_sms) * kRows * D);
@@ -158,17 +202,29 @@ dg_status_t encode_map(CUtensorMap* map, const void* base, int rows, int heads, 
 }
 
 template <int D>
-dg_status_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                   const FwdParams& p, int num_ctas, int max_tiles, cudaStream_t stream,
+dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
+                   const FwdParams& p, int num_clusters, int max_groups, cudaStream_t stream,
                    cudaEvent_t ev_begin, cudaEvent_t ev_end) {
   using S = Shape<D>;
   using C = FwdCfg<D, S::BN, S::NK, S::NV>;
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DG_ERR_CUDA;
-  fwd_kernel<D, S::BN, S::NK, S::NV><<<num_ctas, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
-  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_clusters * p.C);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV>, mk, mv, p) != cudaSuccess)
+    return DG_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return DG_ERR_CUDA;
-  const dim3 cgrid(max_tiles, (kRows + kCombineWarps - 1) / kCombineWarps);
-  combine_kernel<D><<<cgrid, kCombineWarps * 32, 0, stream>>>(p, num_ctas);
+  const dim3 cgrid(max_groups * p.C, (kRows + kCombineWarps - 1) / kCombineWarps);
+  combine_kernel<D><<<cgrid, kCombineWarps * 32, 0, stream>>>(p, num_clusters);
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   return DG_OK;
 }
@@ -220,10 +276,11 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   const int G = num_q_heads / num_kv_heads;
   const int TT = kRows / G;
   const int BN = kv_tile_rows(head_dim);
-  CUtensorMap mq, mk, mv;
-  if (encode_map(&mq, q, total_q, num_q_heads, head_dim, G, TT) != DG_OK ||
-      encode_map(&mk, k, total_kv, num_kv_heads, head_dim, 1, BN) != DG_OK ||
-      encode_map(&mv, v, total_kv, num_kv_heads, head_dim, 1, BN) != DG_OK)
+  const int Ccl = cluster_for(*di, head_dim);
+  CUtensorMap mk, mv;
+  // each CTA of a cluster loads BN / C rows of every K/V tile
+  if (encode_map(&mk, k, total_kv, num_kv_heads, head_dim, 1, BN / Ccl) != DG_OK ||
+      encode_map(&mv, v, total_kv, num_kv_heads, head_dim, 1, BN / Ccl) != DG_OK)
     return DG_ERR_INVALID_ARG;
 
   uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -235,6 +292,7 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.ws.unit_begin = reinterpret_cast<int64_t*>(w + lay.unit_begin);
   p.ws.part_lse = reinterpret_cast<float*>(w + lay.part_lse);
   p.ws.part_o = reinterpret_cast<float*>(w + lay.part_o);
+  p.q = static_cast<const __nv_bfloat16*>(q);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.status = di->status;
@@ -242,20 +300,21 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.G = G;
   p.TT = TT;
   p.window = window;
+  p.C = Ccl;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   build_worklist_kernel<<<1, 1024, 0, stream>>>(cu_q, ctx_len, mode, num_seqs, total_q, total_kv,
-                                                num_kv_heads, TT, BN, window, lay.max_tiles, p.ws,
-                                                p.status);
+                                                num_kv_heads, TT, BN, window, lay.max_tiles, Ccl,
+                                                p.ws, p.status);
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
-  const int num_ctas = num_ctas_for(*di);
+  const int num_clusters = num_clusters_for(*di, head_dim, Ccl);
   cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
   switch (head_dim) {
-    case 64: return launch<64>(mq, mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
-    case 128: return launch<128>(mq, mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
-    default: return launch<256>(mq, mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
+    case 64: return launch<64>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
+    case 128: return launch<128>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
+    default: return launch<256>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
   }
 }
 }  // namespace

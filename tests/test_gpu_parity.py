@@ -118,6 +118,25 @@ def test_ragged_edge_cases(case):
         full_check(wl, batch, window=W, dev=dev, rel=EDGE_REL)
 
 
+@pytest.mark.parametrize("cluster", ["1", "2", "4", "8"])
+def test_cluster_sizes(cluster):
+    """C query tiles of one (sequence, KV head) share each K/V load through TMA
+    multicast; every cluster size gives the oracle's result, including tail
+    groups with fewer than C tiles and windowed ranges that differ per tile."""
+    os.environ["DG_ATTN_CLUSTER"] = cluster
+    try:
+        for seed, seqs, Hq, Hkv, D, windows in (
+                (41, ((300, 256, 1), (0, 333, 0), (1000, 200, 1)), 8, 4, 128, (-1, 50)),
+                (42, ((700, 256, 1), (5, 100, 0)), 16, 2, 256, (-1, 129)),
+                (43, ((64, 500, 1), (0, 260, 0)), 2, 2, 64, (-1, 0, 200))):
+            wl, batch = wls.random_batch(seed, seqs, Hq, Hkv, D, -1)
+            dev = to_dev(batch)
+            for W in windows:
+                full_check(wl, batch, window=W, dev=dev, rel=EDGE_REL)
+    finally:
+        del os.environ["DG_ATTN_CLUSTER"]
+
+
 def test_single_visible_key_is_exact():
     """W = 0, bidirectional: every query sees only itself, so out == v (bf16)."""
     wl, batch = wls.random_batch(7, ((40, 200, 1), (0, 129, 1)), 4, 2, 128, 0)
