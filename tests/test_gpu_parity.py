@@ -137,6 +137,20 @@ def test_cluster_sizes(cluster):
         del os.environ["DG_ATTN_CLUSTER"]
 
 
+@pytest.mark.parametrize("D", [128, 256])
+def test_large_logits(D):
+    """A large softmax scale spreads the scores over hundreds of units: the row
+    maximum keeps growing across KV tiles (lazy O rescale) and many exponents
+    fall far below the bf16 range (the polynomial exp2's clamp)."""
+    wl, batch = wls.random_batch(50 + D, ((3000, 256, 1), (0, 400, 0)), 8, 2, D, -1)
+    dev = to_dev(batch)
+    out, lse = run_gpu(dev, -1, 1.5)
+    ref_o, ref_l = oracle.attention(f64(batch["q"]), f64(batch["k"]), f64(batch["v"]),
+                                    batch["cu_q"].numpy(), batch["ctx_len"].numpy(),
+                                    batch["mode"].numpy(), -1, 1.5)
+    check(f64(out), f64(lse), ref_o, ref_l, f"large logits D={D}", rel=EDGE_REL)
+
+
 def test_single_visible_key_is_exact():
     """W = 0, bidirectional: every query sees only itself, so out == v (bf16)."""
     wl, batch = wls.random_batch(7, ((40, 200, 1), (0, 129, 1)), 4, 2, 128, 0)
