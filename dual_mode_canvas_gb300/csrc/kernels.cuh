@@ -455,8 +455,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // per KV tile g: S[g&1] = Q K^T (A = Q from TMEM), then, one tile later,
     // O += P V with P read from TMEM where it overwrote S[g&1].  MMAs of one
     // thread execute in issue order, so QK(g+2) may reuse the buffer as soon
-    // as PV(g) has been issued.
-    if (lane == 0) {
+    // as PV(g) has been issued.  The whole warp runs this loop with identical
+    // (warp-uniform) operands and one elected lane issues each tcgen05 op:
+    // issuing from a single divergent lane cost ~100 clocks per MMA.
+    {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, BN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, D, 0, 1);
       uint32_t k_stage = 0, k_phase = 0, v_stage = 0, v_phase = 0;
@@ -465,44 +467,44 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       bool ok = true;
       Seg sg;
       while (ok && it.next(sg)) {
-        if (!wait_phase(bar(Cf::B_Q_FULL), seg_i & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_Q_FULL), seg_i & 1, abort_flag, p.status))) { ok = false; break; }
         tc_fence_after();
         const int n = sg.j1 - sg.j0;
         for (int jj = 0; jj <= n && ok; ++jj) {
           if (jj < n) {
             const uint32_t g = gj + jj;
-            if (!wait_phase(bar(Cf::B_K_FULL + k_stage), k_phase, abort_flag, p.status)) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_K_FULL + k_stage), k_phase, abort_flag, p.status))) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_s = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
             const uint32_t k_base = sK + k_stage * Cf::KV_BYTES;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint64_t b = smem_desc_sw128(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-              umma_bf16_ts(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
+              umma_bf16_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            umma_commit(bar(Cf::B_S_FULL + (g & 1)));
-            if (C > 1) umma_commit_multicast(bar(Cf::B_K_EMPTY + k_stage), cta_mask);
-            else umma_commit(bar(Cf::B_K_EMPTY + k_stage));
+            umma_commit_warp(bar(Cf::B_S_FULL + (g & 1)));
+            if (C > 1) umma_commit_multicast_warp(bar(Cf::B_K_EMPTY + k_stage), cta_mask);
+            else umma_commit_warp(bar(Cf::B_K_EMPTY + k_stage));
             if (++k_stage == NK) { k_stage = 0; k_phase ^= 1; }
           }
           if (jj >= 1) {
             const uint32_t g = gj + jj - 1;
             const bool first = (jj == 1);
             if (first && seg_i > 0 &&
-                !wait_phase(bar(Cf::B_O_FREE), (seg_i - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-            if (!wait_phase(bar(Cf::B_P_FULL + (g & 1)), (g >> 1) & 1, abort_flag, p.status) ||
-                !wait_phase(bar(Cf::B_V_FULL + v_stage), v_phase, abort_flag, p.status)) { ok = false; break; }
+                !__all_sync(0xffffffffu, wait_phase(bar(Cf::B_O_FREE), (seg_i - 1) & 1, abort_flag, p.status))) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_P_FULL + (g & 1)), (g >> 1) & 1, abort_flag, p.status) &&
+                                             wait_phase(bar(Cf::B_V_FULL + v_stage), v_phase, abort_flag, p.status))) { ok = false; break; }
             tc_fence_after();
             const uint32_t p_tm = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
             const uint32_t v_base = sV + v_stage * Cf::KV_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
               const uint64_t b = smem_desc_sw128(v_base + kk * 2048, BN * 128, 1024);
-              umma_bf16_ts(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+              umma_bf16_ts_warp(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
             }
-            umma_commit(bar(Cf::B_O_DONE + (g & 1)));
-            if (C > 1) umma_commit_multicast(bar(Cf::B_V_EMPTY + v_stage), cta_mask);
-            else umma_commit(bar(Cf::B_V_EMPTY + v_stage));
+            umma_commit_warp(bar(Cf::B_O_DONE + (g & 1)));
+            if (C > 1) umma_commit_multicast_warp(bar(Cf::B_V_EMPTY + v_stage), cta_mask);
+            else umma_commit_warp(bar(Cf::B_V_EMPTY + v_stage));
             if (++v_stage == NV) { v_stage = 0; v_phase ^= 1; }
           }
         }
@@ -511,7 +513,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         ++seg_i;
       }
       // every MMA issued by this thread has finished before TMEM is released
-      umma_commit(bar(Cf::B_DRAIN));
+      umma_commit_warp(bar(Cf::B_DRAIN));
       drain_wait(bar(Cf::B_DRAIN), 0);
     }
     __syncwarp();
@@ -598,15 +600,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         }
         const float base = (m_use == -INFINITY) ? 0.f : m_use * sl2;
         // p = 2^(s * scale * log2(e) - base), two lanes per fp32x2 instruction;
-        // the row sum runs in four independent fp32x2 accumulators
+        // the row sum runs in four independent fp32x2 accumulators.  With 128
+        // keys per tile the MUFU ex2 rate alone would match the MMA time, so 3
+        // of every 8 pairs take the polynomial path on the FMA pipe.
+        constexpr int kPolyPairs = BN == 128 ? 3 : 0;
         const uint64_t sl2x2 = f32x2(sl2, sl2), nbase2 = f32x2(-base, -base);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int c = 0; c < BN; c += 2) {
-          float t0, t1;
+          float t0, t1, p0, p1;
           f32x2_split(fma_f32x2(f32x2(s[c], s[c + 1]), sl2x2, nbase2), t0, t1);
-          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+          if (((c >> 1) & 7) < kPolyPairs) {
+            exp2_poly_x2(t0, t1, p0, p1);
+          } else {
+            p0 = ex2_approx(t0);
+            p1 = ex2_approx(t1);
+          }
           pk[c / 2] = pack_bf16x2(p0, p1);
           acc[(c >> 1) & 3] = add_f32x2(acc[(c >> 1) & 3], f32x2(p0, p1));
         }

@@ -159,6 +159,35 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Warp-wide forms: every lane of the warp executes them with identical
+// operands; elect.sync picks one lane (the lowest, the same one every time
+// while the warp is converged) that actually issues.
+__device__ __forceinline__ void umma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_multicast_warp(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -280,6 +309,33 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 2^x for a pair of x in [-126, 128) on the FMA pipe (no MUFU): Cody-Waite
+// range reduction x = n + f with n = round(x) (added to and subtracted from
+// 1.5 * 2^23, which leaves n in the low mantissa bits), a degree-3 minimax
+// polynomial for 2^f on [-1/2, 1/2] (coefficients from a Remez fit of the
+// relative error, max 7.5e-5), and n added to the result's exponent field.
+__device__ __forceinline__ void exp2_poly_x2(float x0, float x1, float& p0, float& p1) {
+  const uint64_t magic = f32x2(12582912.f, 12582912.f);
+  const uint64_t x = f32x2(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
+  const uint64_t t = add_f32x2(x, magic);
+  const uint64_t f = sub_f32x2(x, sub_f32x2(t, magic));
+  uint64_t q = fma_f32x2(f, f32x2(0.05517166905792616f, 0.05517166905792616f),
+                         f32x2(0.2426111221932161f, 0.2426111221932161f));
+  q = fma_f32x2(q, f, f32x2(0.6932609854606553f, 0.6932609854606553f));
+  q = fma_f32x2(q, f, f32x2(0.9999280735394012f, 0.9999280735394012f));
+  float q0, q1, t0, t1;
+  f32x2_split(q, q0, q1);
+  f32x2_split(t, t0, t1);
+  p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
+  p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
+}
+
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
