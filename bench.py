@@ -449,13 +449,61 @@ def run_reference(args):
     print(json.dumps(res))
 
 
+def run_accept(args):
+    """The entropy-bounded acceptance step of one denoise step (HBM-bound: one
+    pass over the LM-head logits).  Value: logits bytes / kernel time."""
+    world, rank, local = dist_setup()
+    wl = wls.LOGITS_WORKLOADS[args.workload]
+    binding.load_library()
+    x, cu = wls.make_logits(wl, device="cuda")
+    cu = cu.cuda()
+    rows = wl.rows
+    acc_in = torch.zeros(rows, dtype=torch.uint8, device="cuda")
+    prev = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    stable = torch.zeros(len(wl.canvases), dtype=torch.int32, device="cuda")
+    ws = torch.empty(binding.load_library().dg_accept_workspace_size(rows, wl.vocab),
+                     dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    nsteps = args.warmup + args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(nsteps)]
+    for s_ in range(nsteps):
+        flush.fill_(s_ & 0xFF)
+        binding.accept_step(x, cu, acc_in, prev, stable, 2.0, 3.0, 3, s_, 48, workspace=ws,
+                            events=ev[s_])
+    torch.cuda.synchronize()
+    st = binding.status()
+    if st != binding.DG_OK:
+        raise RuntimeError(f"device status {st}")
+    ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.warmup, nsteps)]
+    tot = replicas.aggregate(float(sum(ms)), 0.0, device="cuda")[0]
+    nbytes = x.numel() * 2 + rows * (4 + 4 + 4 + 1 + 1 + 4)
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    gbs = world * nbytes * args.steps / (tot * 1e-3) / 1e9
+    kgbs = nbytes / (float(np.mean(ms)) * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "entropy-bounded acceptance step GB/s (logits read once)", "value": round(gbs, 1),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded logits, bf16)",
+        "config": {"workload": wl.name, "canvases": list(wl.canvases), "vocab": wl.vocab,
+                   "l2": "flushed before every step (256 MiB write)"},
+        "gpu_launches": 2 * args.steps * world,
+        "roofline": {"bound": "hbm", "achieved": round(kgbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(kgbs / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": src, "kernel": "row_stats_kernel + accept_kernel"}}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="denoise_loop", choices=sorted(wls.WORKLOADS))
+    ap.add_argument("--workload", default="denoise_loop",
+                    choices=sorted(wls.WORKLOADS) + sorted(wls.LOGITS_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
@@ -463,6 +511,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in wls.LOGITS_WORKLOADS:
+        run_accept(args)
     else:
         run_gpu(args)
 

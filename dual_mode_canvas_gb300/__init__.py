@@ -6,4 +6,5 @@ the C ABI of ``include/dg_attn.h``); ``binding`` is a thin ctypes layer over it.
 """
 
 from .binding import (DG_MODE_BIDIRECTIONAL, DG_MODE_CAUSAL, DgAttnError,  # noqa: F401
-                      error_string, forward, load_library, status, version, workspace_size)
+                      accept_step, error_string, forward, load_library, status, version,
+                      workspace_size)

@@ -27,7 +27,8 @@ DG_MODE_CAUSAL = 0
 DG_MODE_BIDIRECTIONAL = 1
 
 EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profiled",
-            "dg_attn_forward_noalloc", "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
+            "dg_attn_forward_noalloc", "dg_accept_workspace_size", "dg_accept_step",
+            "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
 
 _lib = None
 
@@ -62,6 +63,12 @@ def load_library():
     lib.dg_attn_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                             i32, ctypes.c_float, vp, vp, vp]
     lib.dg_attn_forward_noalloc.restype = ctypes.c_int
+    lib.dg_accept_workspace_size.argtypes = [i32, i32]
+    lib.dg_accept_workspace_size.restype = sz
+    f32 = ctypes.c_float
+    lib.dg_accept_step.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, f32, f32, i32, i32, i32,
+                                   vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.dg_accept_step.restype = ctypes.c_int
     lib.dg_attn_status.argtypes = [vp]
     lib.dg_attn_status.restype = ctypes.c_int
     lib.dg_attn_error_string.argtypes = [i32]
@@ -142,3 +149,47 @@ def forward(q, k, v, cu_q, ctx_len, mode, window: int, scale: float, *, out=None
     if rc != DG_OK:
         raise DgAttnError(rc, "dg_attn_forward")
     return out, lse
+
+
+def accept_step(logits, cu_rows, accepted_in, argmax_prev, stable_in, entropy_budget: float,
+                entropy_threshold: float, patience: int, step: int, max_steps: int, *,
+                workspace=None, stream=None, events=None):
+    """Entropy-bounded acceptance of one denoise step through ``dg_accept_step``.
+
+    logits [rows, vocab] bf16, cu_rows [canvases+1] int32, accepted_in [rows]
+    uint8, argmax_prev [rows] int32, stable_in [canvases] int32 (CUDA).  Returns
+    a dict of entropy, confidence, argmax, accepted, stable, converged tensors.
+    ``events=(begin, end)`` are recorded around the call on the stream.
+    """
+    lib = load_library()
+    for name, t, dt in (("logits", logits, torch.bfloat16), ("cu_rows", cu_rows, torch.int32),
+                        ("accepted_in", accepted_in, torch.uint8),
+                        ("argmax_prev", argmax_prev, torch.int32), ("stable_in", stable_in, torch.int32)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    rows, vocab = logits.shape
+    nb = cu_rows.numel() - 1
+    dev = logits.device
+    res = dict(entropy=torch.empty(rows, dtype=torch.float32, device=dev),
+               confidence=torch.empty(rows, dtype=torch.float32, device=dev),
+               argmax=torch.empty(rows, dtype=torch.int32, device=dev),
+               accepted=torch.empty(rows, dtype=torch.uint8, device=dev),
+               stable=torch.empty(nb, dtype=torch.int32, device=dev),
+               converged=torch.empty(nb, dtype=torch.uint8, device=dev))
+    need = lib.dg_accept_workspace_size(rows, vocab)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    sh = _stream_handle(stream)
+    if events is not None:
+        events[0].record(torch.cuda.current_stream() if stream is None else stream)
+    rc = lib.dg_accept_step(_ptr(logits), rows, vocab, _ptr(cu_rows), nb, _ptr(accepted_in),
+                            _ptr(argmax_prev), _ptr(stable_in), float(entropy_budget),
+                            float(entropy_threshold), int(patience), int(step), int(max_steps),
+                            _ptr(res["entropy"]), _ptr(res["confidence"]), _ptr(res["argmax"]),
+                            _ptr(res["accepted"]), _ptr(res["stable"]), _ptr(res["converged"]),
+                            _ptr(workspace), workspace.numel() * workspace.element_size(), sh)
+    if events is not None:
+        events[1].record(torch.cuda.current_stream() if stream is None else stream)
+    if rc != DG_OK:
+        raise DgAttnError(rc, "dg_accept_step")
+    return res

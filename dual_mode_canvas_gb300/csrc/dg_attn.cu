@@ -13,6 +13,7 @@
 
 #include "dg_attn.h"
 #include "kernels.cuh"
+#include "acceptance.cuh"
 
 namespace dg {
 
@@ -364,6 +365,65 @@ extern "C" dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, con
   return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
                       num_kv_heads, head_dim, window, scale, out, lse, di->noalloc_scratch,
                       DG_ATTN_NOALLOC_SCRATCH_BYTES, stream, nullptr, nullptr);
+}
+
+extern "C" size_t dg_accept_workspace_size(int32_t rows, int32_t vocab) {
+  if (rows < 0 || vocab < 1) return 0;
+  const size_t chunks = (static_cast<size_t>(vocab) + kStatChunk - 1) / kStatChunk;
+  return align256(sizeof(RowPartial) * chunks * static_cast<size_t>(rows) + 1);
+}
+
+extern "C" dg_status_t dg_accept_step(const void* logits, int32_t rows, int32_t vocab,
+                                      const int32_t* cu_rows, int32_t num_canvases,
+                                      const uint8_t* accepted_in, const int32_t* argmax_prev,
+                                      const int32_t* stable_in, float entropy_budget,
+                                      float entropy_threshold, int32_t patience, int32_t step,
+                                      int32_t max_steps, float* entropy_out, float* confidence_out,
+                                      int32_t* argmax_out, uint8_t* accepted_out,
+                                      int32_t* stable_out, uint8_t* converged_out, void* workspace,
+                                      size_t workspace_bytes, void* stream_ptr) {
+  if (rows < 0 || vocab < 1 || num_canvases < 0 || patience < 0 || max_steps < 1 || step < 0 ||
+      !std::isfinite(entropy_budget) || entropy_budget < 0.f || !std::isfinite(entropy_threshold))
+    return DG_ERR_INVALID_ARG;
+  if (rows == 0 || num_canvases == 0) return DG_OK;
+  if (!logits || !cu_rows || !accepted_in || !argmax_prev || !stable_in || !entropy_out ||
+      !confidence_out || !argmax_out || !accepted_out || !stable_out || !converged_out)
+    return DG_ERR_INVALID_ARG;
+  if (!aligned(logits, 16)) return DG_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < dg_accept_workspace_size(rows, vocab))
+    return DG_ERR_WORKSPACE;
+  DeviceInfo* di = nullptr;
+  const dg_status_t st = device_info(&di);
+  if (st != DG_OK) return st;
+  const int chunks = (vocab + kStatChunk - 1) / kStatChunk;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  RowPartial* part = static_cast<RowPartial*>(workspace);
+  row_stats_kernel<<<static_cast<unsigned>(rows) * chunks, kStatThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(logits), vocab, chunks, part);
+  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  AcceptParams ap;
+  ap.part = part;
+  ap.chunks = chunks;
+  ap.cu_rows = cu_rows;
+  ap.accepted_in = accepted_in;
+  ap.argmax_prev = argmax_prev;
+  ap.stable_in = stable_in;
+  ap.budget = entropy_budget;
+  ap.tau = entropy_threshold;
+  ap.patience = patience;
+  ap.step = step;
+  ap.max_steps = max_steps;
+  ap.entropy = entropy_out;
+  ap.confidence = confidence_out;
+  ap.argmax = argmax_out;
+  ap.accepted_out = accepted_out;
+  ap.stable_out = stable_out;
+  ap.converged = converged_out;
+  ap.status = di->status;
+  accept_kernel<<<num_canvases, kAcceptThreads, 0, stream>>>(ap);
+  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  return DG_OK;
 }
 
 extern "C" dg_status_t dg_attn_status(void* stream_ptr) {

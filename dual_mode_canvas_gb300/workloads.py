@@ -137,3 +137,42 @@ def random_batch(seed: int, seqs, num_q_heads: int, num_kv_heads: int, head_dim:
     """Ad-hoc batch for edge-case tests: same recipe, caller-chosen shapes."""
     wl = Workload("adhoc", tuple(seqs), num_q_heads, num_kv_heads, head_dim, window, seed)
     return wl, make_batch(wl, device=device, dtype=dtype)
+
+
+# ---------------------------------------------------------------- sampler step
+@dataclass(frozen=True)
+class LogitsWorkload:
+    """LM-head logits of the canvases of one denoise step."""
+    name: str
+    canvases: tuple        # rows per canvas
+    vocab: int
+    seed: int
+    sigma: float = 2.0     # spread of the background logits
+    peak: float = 14.0     # largest bump added to one token per row
+
+    @property
+    def rows(self) -> int:
+        return sum(self.canvases)
+
+
+# 4 canvases of 256 positions (max-num-seqs 4); a 262144-token vocabulary is an
+# assumption (the pages do not give the vocabulary size)
+LOGITS_WORKLOADS = {
+    "accept_small": LogitsWorkload("accept_small", (256, 100, 37), 50001, 20),
+    "accept_step": LogitsWorkload("accept_step", (256, 256, 256, 256), 262144, 21),
+}
+
+
+def make_logits(wl: LogitsWorkload, device="cpu", dtype=torch.bfloat16):
+    """logits [rows, vocab]: sigma * N(0,1) background plus, per row, one token
+    raised by U(0, peak) (so confidences and entropies spread out), drawn in the
+    order background, bump tokens, bump heights; and cu_rows [canvases+1]."""
+    gen = torch.Generator(device=device).manual_seed(wl.seed)
+    x = _randn(gen, (wl.rows, wl.vocab), device) * wl.sigma
+    tok = torch.randint(0, wl.vocab, (wl.rows,), generator=gen, device=device)
+    bump = torch.rand(wl.rows, generator=gen, device=device) * wl.peak
+    x[torch.arange(wl.rows, device=device), tok] += bump
+    cu = [0]
+    for n in wl.canvases:
+        cu.append(cu[-1] + n)
+    return x.to(dtype), torch.tensor(cu, dtype=torch.int32)

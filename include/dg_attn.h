@@ -142,6 +142,45 @@ dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, const void* v,
                                     int32_t head_dim, int32_t window, float scale,
                                     void* out, float* lse, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Entropy-bounded acceptance of one denoise step (DiffusionGemma, agentlenshq
+ * page, "sampling loop and entropy-bounded denoising"; 24-ai.news page, "the
+ * mechanism for deciding finished tokens").  For every canvas position the
+ * LM-head logits give a softmax over the vocabulary; the step computes, per
+ * row, the entropy H (nats), the confidence c (largest probability) and the
+ * argmax (lowest index on ties).  Per canvas, the rows not yet accepted are
+ * ranked by confidence (ties to the lower row) and accepted in that order while
+ * the running entropy sum, accumulated in fp32 in ranking order, stays within
+ * `entropy_budget`; the most confident open row is always accepted.  The canvas
+ * has converged when every argmax equals the previous step's for `patience`
+ * consecutive steps (stable_out = stable_in + 1, or 0 when any argmax changed)
+ * and the mean entropy (fp32 sum in row order, divided by the row count) is
+ * below `entropy_threshold`, or when step + 1 >= max_steps.
+ *
+ *   logits        bf16 device [rows, vocab], row-major, 16-byte aligned
+ *   cu_rows       int32 device [num_canvases+1]: canvas b owns rows
+ *                 cu_rows[b] .. cu_rows[b+1]-1 (at most 1024 rows per canvas;
+ *                 a larger canvas records DG_ERR_INVALID_ARG in the status word)
+ *   accepted_in   uint8 device [rows], 1 = accepted in an earlier step
+ *   argmax_prev   int32 device [rows], the previous step's argmax
+ *   stable_in     int32 device [num_canvases]
+ *   entropy_out, confidence_out  fp32 device [rows];  argmax_out int32 [rows]
+ *   accepted_out  uint8 device [rows] (accepted_in plus this step's acceptances)
+ *   stable_out    int32 device [num_canvases];  converged_out uint8 [num_canvases]
+ *   workspace     >= dg_accept_workspace_size(rows, vocab) bytes, 256-byte aligned
+ */
+size_t dg_accept_workspace_size(int32_t rows, int32_t vocab);
+
+dg_status_t dg_accept_step(const void* logits, int32_t rows, int32_t vocab,
+                           const int32_t* cu_rows, int32_t num_canvases,
+                           const uint8_t* accepted_in, const int32_t* argmax_prev,
+                           const int32_t* stable_in,
+                           float entropy_budget, float entropy_threshold,
+                           int32_t patience, int32_t step, int32_t max_steps,
+                           float* entropy_out, float* confidence_out, int32_t* argmax_out,
+                           uint8_t* accepted_out, int32_t* stable_out, uint8_t* converged_out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, returns the current device's status word (DG_OK if
  * no device-side error was recorded since the last call) and clears it. */
 dg_status_t dg_attn_status(void* stream);

@@ -1,0 +1,109 @@
+"""GPU parity of the entropy-bounded acceptance step (called through the C ABI)
+against the CPU oracle on the same seeded bf16 logits.
+
+Entropy and confidence are compared with the fp64 oracle within a tolerance;
+the argmax is compared exactly (both sides see the same bf16 values; ties go to
+the lower index).  The decisions floating point takes (ranking, acceptance,
+convergence) are checked bit-exactly by running the oracle's decision rules on
+the kernel's own fp32 entropies and confidences, accumulating in fp32 in the
+same order as the kernel.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.acceptance as acc
+from dual_mode_canvas_gb300 import binding
+from dual_mode_canvas_gb300 import workloads as wls
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load_library()
+    yield
+    assert binding.status() == binding.DG_OK
+
+
+def run_and_check(wl, budget, tau, patience, step, max_steps, seed=0, rows_for_oracle=None):
+    x, cu = wl_logits = wls.make_logits(wl, device="cuda")
+    rows = wl.rows
+    rng = np.random.default_rng(seed)
+    acc_in = torch.from_numpy((rng.uniform(size=rows) < 0.25).astype(np.uint8)).cuda()
+    prev = torch.from_numpy(rng.integers(0, wl.vocab, rows).astype(np.int32))
+    H0, c0, a0 = acc.row_stats(x.float().cpu().numpy())
+    # half of the canvases keep every argmax of the previous step
+    nb = len(wl.canvases)
+    cu_h = cu.numpy()
+    for b in range(0, nb, 2):
+        prev[cu_h[b]:cu_h[b + 1]] = torch.from_numpy(a0[cu_h[b]:cu_h[b + 1]].astype(np.int32))
+    stable_in = torch.from_numpy(rng.integers(0, 4, nb).astype(np.int32)).cuda()
+    res = binding.accept_step(x, cu.cuda(), acc_in, prev.cuda(), stable_in, budget, tau, patience,
+                              step, max_steps)
+    torch.cuda.synchronize()
+    assert binding.status() == binding.DG_OK
+    H = res["entropy"].cpu().numpy()
+    c = res["confidence"].cpu().numpy()
+    a = res["argmax"].cpu().numpy()
+    np.testing.assert_allclose(H, H0, rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(c, c0, rtol=1e-4, atol=1e-7)
+    np.testing.assert_array_equal(a, a0)
+    acc_np = acc_in.cpu().numpy().astype(bool)
+    prev_np = prev.numpy()
+    st = stable_in.cpu().numpy()
+    for b in range(nb):
+        r0, r1 = cu_h[b], cu_h[b + 1]
+        exp_acc = acc.accept(H[r0:r1], c[r0:r1], acc_np[r0:r1], np.float32(budget), np.float32)
+        np.testing.assert_array_equal(res["accepted"].cpu().numpy()[r0:r1].astype(bool), exp_acc)
+        cv, sb = acc.converge(a[r0:r1], prev_np[r0:r1], int(st[b]), H[r0:r1], np.float32(tau),
+                              patience, step, max_steps, np.float32)
+        assert bool(res["converged"][b].item()) == cv and int(res["stable"][b].item()) == sb
+    return res
+
+
+@pytest.mark.parametrize("budget", [0.0, 0.5, 4.0, 1e6])
+def test_ragged_canvases_unaligned_vocab(budget):
+    run_and_check(wls.LOGITS_WORKLOADS["accept_small"], budget, 3.0, 2, 5, 48)
+
+
+def test_step_limit_and_threshold():
+    wl = wls.LOGITS_WORKLOADS["accept_small"]
+    run_and_check(wl, 1.0, 100.0, 1, 47, 48, seed=3)   # step limit reached
+    run_and_check(wl, 1.0, 0.0, 0, 0, 48, seed=4)      # threshold never met
+
+
+def test_full_vocab_four_canvases():
+    run_and_check(wls.LOGITS_WORKLOADS["accept_step"], 2.0, 4.0, 3, 10, 48, seed=5)
+
+
+def test_tiny_vocab_and_ties():
+    wl = wls.LogitsWorkload("ties", (5, 3), 9, 30)
+    x = torch.zeros((8, 9), dtype=torch.bfloat16, device="cuda")
+    x[1, 4] = x[1, 7] = 2.0                            # tie: lowest index wins
+    x[2, :] = 1.0                                      # all equal: index 0, entropy ln 9
+    x[3, 8] = 5.0
+    cu = torch.tensor([0, 5, 8], dtype=torch.int32, device="cuda")
+    z8 = torch.zeros(8, dtype=torch.uint8, device="cuda")
+    z32 = torch.zeros(8, dtype=torch.int32, device="cuda")
+    res = binding.accept_step(x, cu, z8, z32, torch.zeros(2, dtype=torch.int32, device="cuda"),
+                              0.1, 1.0, 1, 0, 10)
+    torch.cuda.synchronize()
+    a = res["argmax"].cpu().numpy()
+    assert a[1] == 4 and a[2] == 0 and a[3] == 8
+    assert abs(res["entropy"][2].item() - np.log(9)) < 1e-5
+    # at least one position of each canvas is accepted even with a tiny budget
+    got = res["accepted"].cpu().numpy()
+    assert got[:5].sum() >= 1 and got[5:].sum() >= 1
+
+
+def test_oversized_canvas_sets_status():
+    x = torch.zeros((1100, 16), dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 1100], dtype=torch.int32, device="cuda")
+    z8 = torch.zeros(1100, dtype=torch.uint8, device="cuda")
+    z32 = torch.zeros(1100, dtype=torch.int32, device="cuda")
+    binding.accept_step(x, cu, z8, z32, torch.zeros(1, dtype=torch.int32, device="cuda"), 1.0, 1.0, 1, 0, 4)
+    assert binding.status() == binding.DG_ERR_INVALID_ARG
