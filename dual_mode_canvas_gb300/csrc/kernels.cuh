@@ -44,6 +44,9 @@ constexpr int kVLoadWarp = 6;       // loads the V ring
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitTimeoutNs = 250ull * 1000ull * 1000ull;
 constexpr int kMaxCluster = 8;      // portable cluster size limit
+// Work-split weight of starting a segment, in KV-tile units (every group
+// occupies kSegWeight + its KV tiles in the split).
+constexpr int kSegWeight = 0;
 
 // error codes shared with the host (same values as dg_status_t)
 constexpr int kErrInvalid = 1;
@@ -206,7 +209,7 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
       td.causal = causal ? 1 : 0;
       ws.tiles[static_cast<size_t>(grp) * C + r] = td;
     }
-    ws.unit_begin[grp] = kv_hi / BN - kv_lo / BN + 1;
+    ws.unit_begin[grp] = kSegWeight + kv_hi / BN - kv_lo / BN + 1;
   }
   __syncthreads();
   block_exclusive_scan(ws.unit_begin, num_tiles);
@@ -249,12 +252,15 @@ __device__ __forceinline__ int tile_of_unit(const int64_t* ub, int num_tiles, in
 
 struct Seg {
   int tile;
-  int j0, j1;   // KV-tile range within the tile's range
-  int whole;    // segment covers every KV tile of its tile
+  int j0, j1;   // KV-tile range within the group's range
+  int whole;    // segment covers every KV tile of its group
   int slot;     // partial slot when not whole
 };
 
-// Walks the segments of one CTA's unit range; every role walks the same list.
+// Walks the segments of one cluster's unit range; every role walks the same
+// list.  A group spans units [ub[g], ub[g+1]); its KV tiles are the units from
+// ub[g] + kSegWeight on, so a range that only touches a group's first
+// kSegWeight units yields no segment of it.
 struct SegIter {
   const int64_t* ub;
   int num_tiles;
@@ -262,18 +268,22 @@ struct SegIter {
   int cta;
   bool first;
   __device__ bool next(Seg& sg) {
-    if (u >= u_end) return false;
-    const int t = tile_of_unit(ub, num_tiles, u);
-    const int64_t t0 = ub[t], t1 = ub[t + 1];
-    const int64_t e = u_end < t1 ? u_end : t1;
-    sg.tile = t;
-    sg.j0 = static_cast<int>(u - t0);
-    sg.j1 = static_cast<int>(e - t0);
-    sg.whole = (u == t0 && e == t1) ? 1 : 0;
-    sg.slot = first ? 2 * cta : 2 * cta + 1;
-    u = e;
-    first = false;
-    return true;
+    while (u < u_end) {
+      const int t = tile_of_unit(ub, num_tiles, u);
+      const int64_t r0 = ub[t] + kSegWeight, t1 = ub[t + 1];
+      const int64_t b = u > r0 ? u : r0;
+      const int64_t e = u_end < t1 ? u_end : t1;
+      u = e;
+      if (b >= e) continue;
+      sg.tile = t;
+      sg.j0 = static_cast<int>(b - r0);
+      sg.j1 = static_cast<int>(e - r0);
+      sg.whole = (b == r0 && e == t1) ? 1 : 0;
+      sg.slot = first ? 2 * cta : 2 * cta + 1;
+      first = false;
+      return true;
+    }
+    return false;
   }
 };
 
@@ -425,6 +435,19 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       Seg sg;
       while (ok && it.next(sg)) {
         const TileDesc td = p.ws.tiles[static_cast<size_t>(sg.tile) * C + rank];
+        if (is_k) {
+          // the next segment's Q rows go to L2 while this segment streams, so
+          // the softmax warps load them at L2 latency at the segment switch
+          SegIter look = it;
+          Seg nx;
+          if (look.next(nx)) {
+            const TileDesc tn = p.ws.tiles[static_cast<size_t>(nx.tile) * C + rank];
+            const int ntok = max(tn.n_tok, 1);
+            for (int t = 0; t < ntok; ++t)
+              prefetch_l2_bulk(p.q + (static_cast<size_t>(tn.q_row0 + t) * p.Hq + tn.kvh * G) * D,
+                               static_cast<uint32_t>(G * D * 2));
+          }
+        }
         for (int j = sg.j0; j < sg.j1; ++j) {
           if (!wait_phase(empty0 + 8u * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(full0 + 8u * stage, t_tx);
@@ -528,9 +551,45 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     uint32_t gj = 0;
     int seg_i = 0;
     bool ok = true;
+    // This thread's row of a tile's Q, staged in registers as packed bf16
+    // pairs: the loads of the next segment's row are issued at the start of
+    // this segment's epilogue and land while O is drained.
+    uint32_t qw[D / 2];
+    auto q_issue = [&](const TileDesc& t) {
+      const int ntq = max(t.n_tok, 1);
+      const int hq = t.kvh * G + (r < G * TT ? g_row : 0);
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<size_t>(t.q_row0 + min(t_row, ntq - 1)) * p.Hq + hq) * D);
+#pragma unroll
+      for (int e = 0; e < D / 8; ++e) {
+        const uint4 x = __ldg(src + e);
+        qw[4 * e + 0] = x.x; qw[4 * e + 1] = x.y; qw[4 * e + 2] = x.z; qw[4 * e + 3] = x.w;
+      }
+    };
+    // registers -> TMEM Q columns; the MMA warp may start QK^T after this
+    auto q_commit = [&]() {
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tmem_st32(lane_base + Cf::TM_Q + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&qw[c * 32]));
+      tc_fence_before();
+      mbar_arrive(bar(Cf::B_Q_FULL));
+    };
     Seg sg;
-    while (ok && it.next(sg)) {
+    bool have = it.next(sg);
+    if (have) {
+      q_issue(p.ws.tiles[static_cast<size_t>(sg.tile) * C + rank]);
+      q_commit();
+    }
+    // With head_dim 256 the register file has room to stage the next row
+    // during the epilogue; smaller head dims load it at the segment start.
+    constexpr bool kStageQ = (D == 256);
+    bool q_loaded = true;  // the first segment's Q is already in TMEM
+    while (ok && have) {
       const TileDesc td = p.ws.tiles[static_cast<size_t>(sg.tile) * C + rank];
+      if (!q_loaded) {
+        q_issue(td);
+        q_commit();
+      }
       // a rank without a tile in this group (n_tok == 0) still runs the
       // pipeline on its neighbour's rows so the cluster stays in lockstep,
       // but writes nothing
@@ -543,26 +602,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       const int i_lo = td.pos0, i_hi = td.pos0 + nt - 1;
       const int lo_all = W < 0 ? INT32_MIN / 2 : i_hi - W;  // largest row lower bound
       const int hi_all = min(td.L - 1, td.causal ? i_lo : (W < 0 ? td.L - 1 : i_lo + W));
-      const int h = td.kvh * G + (r < G * TT ? g_row : 0);
-
-      // Q row -> TMEM (the previous segment's MMAs finished before its epilogue)
-      {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + (static_cast<size_t>(td.q_row0 + tq) * p.Hq + h) * D);
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t w[32];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint4 x = __ldg(src + c * 8 + e);
-            w[4 * e + 0] = x.x; w[4 * e + 1] = x.y; w[4 * e + 2] = x.z; w[4 * e + 3] = x.w;
-          }
-          tmem_st32(lane_base + Cf::TM_Q + c * 32, w);
-        }
-        tc_fence_before();
-        mbar_arrive(bar(Cf::B_Q_FULL));
-      }
-
       float m_run = -INFINITY, l_run = 0.f;
       const int n = sg.j1 - sg.j0;
       for (int jj = 0; jj < n; ++jj) {
@@ -659,6 +698,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         }
       }
       tc_fence_after();
+      Seg nx;
+      SegIter look = it;
+      const bool more = kStageQ && look.next(nx);
+      if (more) q_issue(p.ws.tiles[static_cast<size_t>(nx.tile) * C + rank]);
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse_v = l_run > 0.f ? m_run * p.scale + logf(l_run) : -INFINITY;
       if (sg.whole) {
@@ -694,10 +737,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         }
         p.ws.part_lse[static_cast<size_t>(sg.slot) * kRows + r] = lse_v;
       }
+      if (more) q_commit();
       tc_fence_before();
       mbar_arrive(bar(Cf::B_O_FREE));
       gj += n;
       ++seg_i;
+      have = it.next(sg);
+      q_loaded = more;
     }
   }
 
@@ -726,7 +772,7 @@ combine_kernel(const FwdParams p, int num_clusters) {
   const int64_t U = hdr->total_units;
   const int P = active_ctas(num_clusters, U);
   const int64_t T0 = p.ws.unit_begin[grp], T1 = p.ws.unit_begin[grp + 1];
-  const int c_lo = cta_of_unit(T0, U, P);
+  const int c_lo = cta_of_unit(T0 + kSegWeight, U, P);  // clusters holding KV tiles of the group
   const int c_hi = cta_of_unit(T1 - 1, U, P);
   if (c_lo == c_hi) return;  // written directly by one cluster
   const TileDesc td = p.ws.tiles[blockIdx.x];

@@ -108,6 +108,14 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) of global
+// memory into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
