@@ -49,92 +49,145 @@ __device__ __forceinline__ void merge_stats(float& m, float& s, float& t, int& a
   const float mn = fmaxf(m, m2);
   const float d1 = m - mn, d2 = m2 - mn;
   const float e1 = exp2f(d1 * kLog2e), e2 = exp2f(d2 * kLog2e);
-  t = e1 * (t + d1 * s) + e2 * (t2 + d2 * s2);
+  // a side whose weight underflows to 0 drops out: its d * s may overflow to
+  // -inf (a chunk of masked logits has m = the lowest finite value), and
+  // 0 * -inf would be NaN
+  float tn = 0.f;
+  if (e1 > 0.f) tn += e1 * (t + d1 * s);
+  if (e2 > 0.f) tn += e2 * (t2 + d2 * s2);
+  t = tn;
   s = e1 * s + e2 * s2;
   if (m2 > m || (m2 == m && a2 < a)) a = a2;
   m = mn;
 }
 
-__global__ void __launch_bounds__(kStatThreads, 3)
+// Chunks are laid out from the 16-byte boundary at or before the row's first
+// logit, so every full 8-logit group is one aligned vector load whatever the
+// vocabulary size or the buffer's alignment: chunk c of a row covers row
+// positions [c K - off, (c + 1) K - off), off = the row start's misalignment
+// in logits (0..7).  `chunks` must cover vocab + off.
+__global__ void __launch_bounds__(kStatThreads, 4)
 row_stats_kernel(const __nv_bfloat16* __restrict__ logits, int vocab, int chunks,
                  RowPartial* __restrict__ part) {
   const int row = blockIdx.x / chunks, chunk = blockIdx.x - row * chunks;
   const int64_t base = static_cast<int64_t>(row) * vocab;
-  const int lo = chunk * kStatChunk;
-  const int hi = min(vocab, lo + kStatChunk);
+  const int off = static_cast<int>(((reinterpret_cast<uintptr_t>(logits) >> 1) + base) & 7);
   const int tid = threadIdx.x;
-  constexpr int kIters = kStatChunk / (kStatThreads * kStatVec);  // 8 loads per thread
-  // pass 1: the thread's values in registers, its max and first argmax
+  constexpr int kIters = kStatChunk / (kStatThreads * kStatVec);  // 8 vectors per thread
+  // row position of the first logit of vector k of this thread
+  auto first = [&](int k) { return chunk * kStatChunk - off + (k * kStatThreads + tid) * kStatVec; };
+  // The lowest finite bf16: -inf logits (and positions outside the row) are
+  // raised to it, so x - M stays finite and e * (x - M) is exactly 0.
+  constexpr uint32_t kFloor2 = 0xFF7FFF7Fu;
+  // pass 1a: every load of the thread is issued before any value is used
   uint4 v[kIters];
-  float m = -INFINITY;
-  int a = INT32_MAX;
+  bool has_data = false;
 #pragma unroll
   for (int k = 0; k < kIters; ++k) {
-    const int e0 = lo + (k * kStatThreads + tid) * kStatVec;
-    if (e0 + kStatVec <= hi && ((base + e0) & 7) == 0) {
-      v[k] = __ldg(reinterpret_cast<const uint4*>(logits + base + e0));
+    const int r0 = first(k);
+    has_data |= (r0 + kStatVec > 0 && r0 < vocab);
+    if (r0 >= 0 && r0 + kStatVec <= vocab) {
+      v[k] = __ldg(reinterpret_cast<const uint4*>(logits + base + r0));
     } else {
-      // ragged tail or a row that does not start 16-byte aligned: element loads, pad with -inf
+      // the row's first or last group: element loads of the positions inside the row
       uint32_t w[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int i0 = e0 + 2 * j, i1 = i0 + 1;
-        const unsigned short b0 = i0 < hi ? __bfloat16_as_ushort(logits[base + i0]) : 0xFF80u;
-        const unsigned short b1 = i1 < hi ? __bfloat16_as_ushort(logits[base + i1]) : 0xFF80u;
+        const int i0 = r0 + 2 * j, i1 = i0 + 1;
+        const unsigned short b0 = (i0 >= 0 && i0 < vocab) ? __bfloat16_as_ushort(logits[base + i0]) : 0xFF80u;
+        const unsigned short b1 = (i1 >= 0 && i1 < vocab) ? __bfloat16_as_ushort(logits[base + i1]) : 0xFF80u;
         w[j] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
       }
       v[k] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+  }
+  // pass 1b: clamp and the thread's max (packed pairs)
+  uint32_t mx2 = kFloor2;
+#pragma unroll
+  for (int k = 0; k < kIters; ++k) {
+    v[k].x = max_bf16x2(v[k].x, kFloor2);
+    v[k].y = max_bf16x2(v[k].y, kFloor2);
+    v[k].z = max_bf16x2(v[k].z, kFloor2);
+    v[k].w = max_bf16x2(v[k].w, kFloor2);
+    mx2 = max_bf16x2(mx2, max_bf16x2(max_bf16x2(v[k].x, v[k].y), max_bf16x2(v[k].z, v[k].w)));
+  }
+  // a thread with no position inside the row drops out
+  const float mloc = has_data ? fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xFFFF0000u))
+                              : -INFINITY;
+  // block maximum M (plain max, no exponentials)
+  __shared__ float red_m[kStatThreads / 32];
+  __shared__ float red_s[kStatThreads / 32], red_t[kStatThreads / 32];
+  __shared__ int red_a[kStatThreads / 32];
+  const int warp = tid >> 5, lane = tid & 31;
+  float M = mloc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red_m[warp] = M;
+  __syncthreads();
+  M = red_m[0];
+#pragma unroll
+  for (int w = 1; w < kStatThreads / 32; ++w) M = fmaxf(M, red_m[w]);
+  // pass 2 (registers only) against M, two lanes per fp32x2 instruction:
+  // s = sum e, t = sum e * (x - M), e = 2^((x - M) log2 e)
+  const uint64_t m2x = f32x2(M, M), l2e = f32x2(kLog2e, kLog2e);
+  uint64_t s2 = 0ull, t2 = 0ull;
+#pragma unroll
+  for (int k = 0; k < kIters; ++k) {
     const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float x0 = __uint_as_float(w[j] << 16), x1 = __uint_as_float(w[j] & 0xFFFF0000u);
-      const int i0 = e0 + 2 * j;
-      if (x0 > m) { m = x0; a = i0; }
-      if (x1 > m) { m = x1; a = i0 + 1; }
+      const uint64_t d = sub_f32x2(f32x2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u)), m2x);
+      float y0, y1;
+      f32x2_split(mul_f32x2(d, l2e), y0, y1);
+      const uint64_t e = f32x2(ex2_approx(y0), ex2_approx(y1));
+      s2 = add_f32x2(s2, e);
+      t2 = fma_f32x2(e, d, t2);
     }
   }
-  // pass 2 (registers only): s and t relative to the thread's max
-  float s = 0.f, t = 0.f;
-  if (m > -INFINITY) {
-    const float nm = -m * kLog2e;
+  float s0, s1, t0, t1;
+  f32x2_split(s2, s0, s1);
+  f32x2_split(t2, t0, t1);
+  float s = has_data ? s0 + s1 : 0.f, t = has_data ? t0 + t1 : 0.f;
+  // first index of M: only threads holding M scan their values, in index
+  // order (fully unrolled so the values stay in registers)
+  int a = INT32_MAX;
+  if (mloc == M) {
+    const uint32_t mb = __float_as_uint(M) >> 16;
+    const uint32_t mm2 = mb | (mb << 16);
 #pragma unroll
-    for (int k = 0; k < kIters; ++k) {
+    for (int k = kIters - 1; k >= 0; --k) {
       const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      const int e0 = first(k);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float x0 = __uint_as_float(w[j] << 16), x1 = __uint_as_float(w[j] & 0xFFFF0000u);
-        const float e0 = ex2_approx(fmaf(x0, kLog2e, nm)), e1 = ex2_approx(fmaf(x1, kLog2e, nm));
-        s += e0 + e1;
-        // x - m is clamped so that padding (-inf) gives 0 * -1000 = 0, not 0 * -inf
-        t = fmaf(e0, fmaxf(x0 - m, -1000.f), t);
-        t = fmaf(e1, fmaxf(x1 - m, -1000.f), t);
+      for (int j = 3; j >= 0; --j) {
+        const uint32_t hit = eq_bf16x2(w[j], mm2);
+        if (hit) a = e0 + 2 * j + ((hit & 1u) ? 0 : 1);
       }
     }
   }
-  // block reduction: warps by shuffles, then warp 0 over the warp results
+  // block sums and the lowest index of M
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
-    const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
-    merge_stats(m, s, t, a, m2, s2, t2, a2);
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    t += __shfl_xor_sync(0xffffffffu, t, o);
+    a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
   }
-  __shared__ RowPartial red[kStatThreads / 32];
-  const int warp = tid >> 5, lane = tid & 31;
-  if (lane == 0) red[warp] = RowPartial{m, s, t, a};
+  if (lane == 0) {
+    red_s[warp] = s;
+    red_t[warp] = t;
+    red_a[warp] = a;
+  }
   __syncthreads();
-  if (warp == 0) {
-    RowPartial r = lane < kStatThreads / 32 ? red[lane] : RowPartial{-INFINITY, 0.f, 0.f, INT32_MAX};
-    m = r.m; s = r.s; t = r.t; a = r.arg;
+  if (tid == 0) {
+    float S = 0.f, T = 0.f;
+    int A = INT32_MAX;
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
-      const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
-      merge_stats(m, s, t, a, m2, s2, t2, a2);
+    for (int w = 0; w < kStatThreads / 32; ++w) {
+      S += red_s[w];
+      T += red_t[w];
+      A = min(A, red_a[w]);
     }
-    if (lane == 0) part[blockIdx.x] = RowPartial{m, s, t, a};
+    part[blockIdx.x] = S > 0.f ? RowPartial{M, S, T, A} : RowPartial{-INFINITY, 0.f, 0.f, INT32_MAX};
   }
 }
 

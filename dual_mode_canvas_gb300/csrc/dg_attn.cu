@@ -302,6 +302,8 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.TT = TT;
   p.window = window;
   p.C = Ccl;
+  p.debug_skip_k_load = -1;
+  if (const char* e = std::getenv("DG_ATTN_DEBUG_SKIP_K_LOAD")) p.debug_skip_k_load = std::atoi(e);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
 
@@ -367,9 +369,18 @@ extern "C" dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, con
                       DG_ATTN_NOALLOC_SCRATCH_BYTES, stream, nullptr, nullptr);
 }
 
+namespace {
+// row statistics chunks per row: rows of a vocabulary that is not a multiple of
+// 8 start up to 7 logits past a 16-byte boundary, and the chunks start there
+int stat_chunks(int32_t vocab) {
+  const int64_t span = static_cast<int64_t>(vocab) + (vocab % 8 ? 7 : 0);
+  return static_cast<int>((span + kStatChunk - 1) / kStatChunk);
+}
+}  // namespace
+
 extern "C" size_t dg_accept_workspace_size(int32_t rows, int32_t vocab) {
   if (rows < 0 || vocab < 1) return 0;
-  const size_t chunks = (static_cast<size_t>(vocab) + kStatChunk - 1) / kStatChunk;
+  const size_t chunks = static_cast<size_t>(stat_chunks(vocab));
   return align256(sizeof(RowPartial) * chunks * static_cast<size_t>(rows) + 1);
 }
 
@@ -396,7 +407,7 @@ extern "C" dg_status_t dg_accept_step(const void* logits, int32_t rows, int32_t 
   DeviceInfo* di = nullptr;
   const dg_status_t st = device_info(&di);
   if (st != DG_OK) return st;
-  const int chunks = (vocab + kStatChunk - 1) / kStatChunk;
+  const int chunks = stat_chunks(vocab);
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   RowPartial* part = static_cast<RowPartial*>(workspace);
   row_stats_kernel<<<static_cast<unsigned>(rows) * chunks, kStatThreads, 0, stream>>>(

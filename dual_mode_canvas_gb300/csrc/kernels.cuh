@@ -44,9 +44,10 @@ constexpr int kVLoadWarp = 6;       // loads the V ring
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitTimeoutNs = 250ull * 1000ull * 1000ull;
 constexpr int kMaxCluster = 8;      // portable cluster size limit
-// Work-split weight of starting a segment, in KV-tile units (every group
-// occupies kSegWeight + its KV tiles in the split).
-constexpr int kSegWeight = 0;
+// Work-split weight of starting a segment (Q load, pipeline fill, epilogue),
+// in KV-tile units: every group occupies kSegWeight + (its KV tiles) units of
+// the split, the first kSegWeight of them carrying no KV tile.
+constexpr int kSegWeight = 8;
 
 // error codes shared with the host (same values as dg_status_t)
 constexpr int kErrInvalid = 1;
@@ -86,6 +87,9 @@ struct FwdParams {
   float* lse;
   int* status;
   int Hq, G, TT, window, C;
+  // >= 0: the K loader skips the TMA load of this (per-CTA) KV tile, so the
+  // MMA warp's bounded wait for it expires (tests of the timeout path)
+  int debug_skip_k_load;
   float scale, scale_log2;
 };
 
@@ -431,6 +435,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;  // per stage: a load was issued / its phase
+      int loads = 0;
       bool ok = true;
       Seg sg;
       while (ok && it.next(sg)) {
@@ -450,6 +455,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         }
         for (int j = sg.j0; j < sg.j1; ++j) {
           if (!wait_phase(empty0 + 8u * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (is_k && loads++ == p.debug_skip_k_load) {
+            if (++stage == static_cast<uint32_t>(NS)) { stage = 0; phase ^= 1; }
+            continue;
+          }
           mbar_arrive_expect_tx(full0 + 8u * stage, t_tx);
           const int row = td.kv_row0 + (td.kt_first + j) * BN + rank * slice;
           const uint32_t dst = ring + stage * Cf::KV_BYTES + rank * slice * 128;

@@ -317,6 +317,28 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Lane-wise max of two packed bf16 pairs.
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Bit 0: lower bf16 of a equals lower of b; bit 1: upper equals upper.
+__device__ __forceinline__ uint32_t eq_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t lo, hi;
+  asm("{\n\t.reg .pred pl, ph;\n\t"
+      "setp.eq.bf16x2 pl|ph, %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, pl;\n\t"
+      "selp.u32 %1, 2, 0, ph;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(a), "r"(b));
+  return lo | hi;
+}
 __device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));

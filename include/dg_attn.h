@@ -157,7 +157,10 @@ dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, const void* v,
  * and the mean entropy (fp32 sum in row order, divided by the row count) is
  * below `entropy_threshold`, or when step + 1 >= max_steps.
  *
- *   logits        bf16 device [rows, vocab], row-major, 16-byte aligned
+ *   logits        bf16 device [rows, vocab], row-major, 16-byte aligned; -inf
+ *                 entries are masked tokens (probability 0), NaN is not allowed;
+ *                 a row needs at least one logit above the lowest finite bf16
+ *                 (otherwise it has no distribution and its outputs are unspecified)
  *   cu_rows       int32 device [num_canvases+1]: canvas b owns rows
  *                 cu_rows[b] .. cu_rows[b+1]-1 (at most 1024 rows per canvas;
  *                 a larger canvas records DG_ERR_INVALID_ARG in the status word)

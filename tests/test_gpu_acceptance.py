@@ -107,3 +107,35 @@ def test_oversized_canvas_sets_status():
     z32 = torch.zeros(1100, dtype=torch.int32, device="cuda")
     binding.accept_step(x, cu, z8, z32, torch.zeros(1, dtype=torch.int32, device="cuda"), 1.0, 1.0, 1, 0, 4)
     assert binding.status() == binding.DG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("vocab", [16383, 16385, 32771, 40000])
+def test_chunk_edges_ties_and_masked_logits(vocab):
+    """Vocabularies on both sides of a chunk multiple (rows start at every
+    misalignment), maxima at the first / last position, ties across chunks
+    and rows with -inf (masked) logits; statistics against the oracle."""
+    g = torch.Generator().manual_seed(vocab)
+    rows = 9
+    x = (torch.randn(rows, vocab, generator=g) * 2).to(torch.bfloat16)
+    x[0, vocab - 1] = 30.0                         # max at the last position
+    x[1, 0] = 30.0                                 # max at the first position
+    p_tie = min(16383, vocab // 2)
+    x[2, p_tie] = x[2, vocab - 2] = 30.0           # tie across chunks: the lower wins
+    x[3, 5] = x[3, 16390 % vocab] = x[3, vocab - 1] = 25.0
+    x[4, vocab // 2:] = float("-inf")              # upper half masked
+    x[5, :] = float("-inf")
+    x[5, [3, vocab // 3, vocab - 4]] = torch.tensor([1.0, 2.0, 2.0], dtype=torch.bfloat16)
+    x[6, :] = 0.0                                  # uniform: entropy ln V, argmax 0
+    xd = x.cuda()
+    cu = torch.tensor([0, rows], dtype=torch.int32, device="cuda")
+    z8 = torch.zeros(rows, dtype=torch.uint8, device="cuda")
+    z32 = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    res = binding.accept_step(xd, cu, z8, z32, torch.zeros(1, dtype=torch.int32, device="cuda"),
+                              1.0, 1.0, 1, 0, 10)
+    torch.cuda.synchronize()
+    assert binding.status() == binding.DG_OK
+    H0, c0, a0 = acc.row_stats(x.float().numpy())
+    np.testing.assert_allclose(res["entropy"].cpu().numpy(), H0, rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(res["confidence"].cpu().numpy(), c0, rtol=1e-4, atol=1e-7)
+    np.testing.assert_array_equal(res["argmax"].cpu().numpy(), a0)
+    assert a0[2] == p_tie and a0[5] == vocab // 3 and a0[6] == 0
