@@ -27,7 +27,8 @@ DG_MODE_CAUSAL = 0
 DG_MODE_BIDIRECTIONAL = 1
 
 EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profiled",
-            "dg_attn_forward_noalloc", "dg_accept_workspace_size", "dg_accept_step",
+            "dg_attn_forward_noalloc", "dg_attn_forward_paged", "dg_attn_forward_paged_profiled",
+            "dg_accept_workspace_size", "dg_accept_step",
             "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
 
 _lib = None
@@ -63,6 +64,12 @@ def load_library():
     lib.dg_attn_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                             i32, ctypes.c_float, vp, vp, vp]
     lib.dg_attn_forward_noalloc.restype = ctypes.c_int
+    lib.dg_attn_forward_paged.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, i32, vp, vp, vp, i32,
+                                          i32, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, sz,
+                                          vp]
+    lib.dg_attn_forward_paged.restype = ctypes.c_int
+    lib.dg_attn_forward_paged_profiled.argtypes = lib.dg_attn_forward_paged.argtypes + [vp, vp]
+    lib.dg_attn_forward_paged_profiled.restype = ctypes.c_int
     lib.dg_accept_workspace_size.argtypes = [i32, i32]
     lib.dg_accept_workspace_size.restype = sz
     f32 = ctypes.c_float
@@ -148,6 +155,61 @@ def forward(q, k, v, cu_q, ctx_len, mode, window: int, scale: float, *, out=None
         rc = lib.dg_attn_forward_profiled(*args, events[0].cuda_event, events[1].cuda_event)
     if rc != DG_OK:
         raise DgAttnError(rc, "dg_attn_forward")
+    return out, lse
+
+
+def forward_paged(q, k_new, v_new, k_cache, v_cache, block_table, cu_q, ctx_len, mode,
+                  window: int, scale: float, *, out=None, lse=None, workspace=None, stream=None,
+                  return_lse: bool = True, events=None):
+    """Dual-mode attention over a paged KV cache through ``dg_attn_forward_paged``.
+
+    k_cache / v_cache [num_pages, page_size, Hkv, D] bf16, block_table
+    [B, max_pages_per_seq] int32; k_new / v_new [total_q, Hkv, D] bf16 (or
+    both None) are written into the cache at the query tokens' positions
+    first.  Other arguments as for ``forward``.  Returns ``(out, lse)``.
+    """
+    lib = load_library()
+    checks = [("q", q, torch.bfloat16), ("k_cache", k_cache, torch.bfloat16),
+              ("v_cache", v_cache, torch.bfloat16), ("block_table", block_table, torch.int32),
+              ("cu_q", cu_q, torch.int32), ("ctx_len", ctx_len, torch.int32),
+              ("mode", mode, torch.uint8)]
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new must both be given or both be None")
+    if k_new is not None:
+        checks += [("k_new", k_new, torch.bfloat16), ("v_new", v_new, torch.bfloat16)]
+    for name, t, dt in checks:
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    total_q, Hq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or Dk != D:
+        raise ValueError("k_cache and v_cache must both be [num_pages, page_size, Hkv, D]")
+    if k_new is not None and (tuple(k_new.shape) != (total_q, Hkv, D) or
+                              tuple(v_new.shape) != (total_q, Hkv, D)):
+        raise ValueError("k_new and v_new must be [total_q, Hkv, D]")
+    B = ctx_len.numel()
+    if cu_q.numel() != B + 1 or mode.numel() != B or block_table.dim() != 2 or \
+            block_table.shape[0] != B:
+        raise ValueError("cu_q [B+1], mode [B] and block_table [B, max_pages] required")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    need = lib.dg_attn_workspace_size(B, total_q, Hq, Hkv, D)
+    if need == 0:
+        raise DgAttnError(DG_ERR_INVALID_ARG, "dg_attn_workspace_size")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    args = (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), num_pages, page_size,
+            _ptr(block_table), block_table.shape[1], _ptr(cu_q), _ptr(ctx_len), _ptr(mode), B,
+            total_q, Hq, Hkv, D, int(window), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if events is None:
+        rc = lib.dg_attn_forward_paged(*args)
+    else:
+        rc = lib.dg_attn_forward_paged_profiled(*args, events[0].cuda_event, events[1].cuda_event)
+    if rc != DG_OK:
+        raise DgAttnError(rc, "dg_attn_forward_paged")
     return out, lse
 
 

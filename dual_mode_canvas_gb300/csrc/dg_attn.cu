@@ -247,12 +247,15 @@ extern "C" size_t dg_attn_workspace_size(int32_t num_seqs, int32_t total_q, int3
 }
 
 namespace {
+// `pg` null: contiguous K/V (k, v, total_kv); otherwise the paged cache it
+// describes (k, v unused).
 dg_status_t forward_impl(const void* q, const void* k, const void* v, const int32_t* cu_q,
                          const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
                          int32_t total_q, int32_t total_kv, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale,
                          void* out, float* lse, void* workspace, size_t workspace_bytes,
-                         void* stream_ptr, void* ev_begin, void* ev_end) {
+                         void* stream_ptr, void* ev_begin, void* ev_end,
+                         const PagedArgs* pg = nullptr) {
   if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim))
     return (num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
             num_q_heads / num_kv_heads > kRows) || (head_dim > 0 && head_dim != 64 &&
@@ -262,9 +265,10 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   if (window < -1 || total_kv < 0 || !(scale > 0.f) || !std::isfinite(scale)) return DG_ERR_INVALID_ARG;
   if (num_seqs == 0) return total_q == 0 ? DG_OK : DG_ERR_INVALID_ARG;
   if (total_q == 0) return DG_OK;
-  if (total_kv < total_q) return DG_ERR_INVALID_ARG;
-  if (!q || !k || !v || !cu_q || !ctx_len || !mode || !out) return DG_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+  if (!pg && total_kv < total_q) return DG_ERR_INVALID_ARG;
+  if (!pg && (!k || !v || !aligned(k, 16) || !aligned(v, 16))) return DG_ERR_INVALID_ARG;
+  if (!q || !cu_q || !ctx_len || !mode || !out) return DG_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) ||
       !aligned(cu_q, 4) || !aligned(ctx_len, 4) || (lse && !aligned(lse, 4)))
     return DG_ERR_INVALID_ARG;
 
@@ -279,9 +283,15 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   const int BN = kv_tile_rows(head_dim);
   const int Ccl = cluster_for(*di, head_dim);
   CUtensorMap mk, mv;
-  // each CTA of a cluster loads BN / C rows of every K/V tile
-  if (encode_map(&mk, k, total_kv, num_kv_heads, head_dim, 1, BN / Ccl) != DG_OK ||
-      encode_map(&mv, v, total_kv, num_kv_heads, head_dim, 1, BN / Ccl) != DG_OK)
+  // each CTA of a cluster loads BN / C rows of every K/V tile; from a paged
+  // cache in boxes of at most one page
+  const int slice = BN / Ccl;
+  const int box = pg ? std::min(1 << pg->page_shift, slice) : slice;
+  const void* kmap = pg ? pg->k_cache : k;
+  const void* vmap = pg ? pg->v_cache : v;
+  const int map_rows = pg ? (pg->num_pages << pg->page_shift) : total_kv;
+  if (encode_map(&mk, kmap, map_rows, num_kv_heads, head_dim, 1, box) != DG_OK ||
+      encode_map(&mv, vmap, map_rows, num_kv_heads, head_dim, 1, box) != DG_OK)
     return DG_ERR_INVALID_ARG;
 
   uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -302,15 +312,27 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.TT = TT;
   p.window = window;
   p.C = Ccl;
+  p.block_table = pg ? pg->block_table : nullptr;
+  p.page_shift = pg ? pg->page_shift : 0;
+  p.page_box = box;
   p.debug_skip_k_load = -1;
   if (const char* e = std::getenv("DG_ATTN_DEBUG_SKIP_K_LOAD")) p.debug_skip_k_load = std::atoi(e);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  build_worklist_kernel<<<1, 1024, 0, stream>>>(cu_q, ctx_len, mode, num_seqs, total_q, total_kv,
-                                                num_kv_heads, TT, BN, window, lay.max_tiles, Ccl,
-                                                p.ws, p.status);
+  PagedArgs pa = {};
+  int append_ctas = 0;
+  if (pg) {
+    pa = *pg;
+    if (pa.k_new) {
+      const int64_t units = 2ll * total_q * num_kv_heads * head_dim / 8;
+      append_ctas = static_cast<int>(std::min<int64_t>((units + 1023) / 1024, 2ll * di->num_sms));
+    }
+  }
+  build_worklist_kernel<<<1 + append_ctas, 1024, 0, stream>>>(
+      cu_q, ctx_len, mode, num_seqs, total_q, pg ? INT32_MAX : total_kv, num_kv_heads, TT, BN,
+      window, lay.max_tiles, Ccl, p.ws, pa, p.status);
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   const int num_clusters = num_clusters_for(*di, head_dim, Ccl);
   cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
@@ -367,6 +389,70 @@ extern "C" dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, con
   return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
                       num_kv_heads, head_dim, window, scale, out, lse, di->noalloc_scratch,
                       DG_ATTN_NOALLOC_SCRATCH_BYTES, stream, nullptr, nullptr);
+}
+
+namespace {
+dg_status_t forward_paged(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                          void* v_cache, int32_t num_pages, int32_t page_size,
+                          const int32_t* block_table, int32_t max_pages_per_seq,
+                          const int32_t* cu_q, const int32_t* ctx_len, const uint8_t* mode,
+                          int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale,
+                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream, void* ev_begin, void* ev_end) {
+  if (page_size < 8 || page_size > 65536 || (page_size & (page_size - 1)) != 0)
+    return DG_ERR_INVALID_ARG;
+  if (num_pages < 1 || static_cast<int64_t>(num_pages) * page_size > INT32_MAX)
+    return DG_ERR_INVALID_ARG;
+  if (max_pages_per_seq < 1 || num_seqs < 0 ||
+      static_cast<int64_t>(num_seqs) * max_pages_per_seq > INT32_MAX)
+    return DG_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache || !block_table || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_table, 4))
+    return DG_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return DG_ERR_INVALID_ARG;
+  if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))) return DG_ERR_INVALID_ARG;
+  PagedArgs pg;
+  pg.block_table = block_table;
+  pg.bt_stride = max_pages_per_seq;
+  pg.page_shift = 0;
+  while ((1 << pg.page_shift) < page_size) ++pg.page_shift;
+  pg.num_pages = num_pages;
+  pg.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  pg.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  pg.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  pg.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  pg.Hkv = num_kv_heads;
+  pg.D = head_dim;
+  return forward_impl(q, nullptr, nullptr, cu_q, ctx_len, mode, num_seqs, total_q, 0, num_q_heads,
+                      num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
+                      stream, ev_begin, ev_end, &pg);
+}
+}  // namespace
+
+extern "C" dg_status_t dg_attn_forward_paged(
+    const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    int32_t num_pages, int32_t page_size, const int32_t* block_table, int32_t max_pages_per_seq,
+    const int32_t* cu_q, const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
+    int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t window,
+    float scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return forward_paged(q, k_new, v_new, k_cache, v_cache, num_pages, page_size, block_table,
+                       max_pages_per_seq, cu_q, ctx_len, mode, num_seqs, total_q, num_q_heads,
+                       num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
+                       stream, nullptr, nullptr);
+}
+
+extern "C" dg_status_t dg_attn_forward_paged_profiled(
+    const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    int32_t num_pages, int32_t page_size, const int32_t* block_table, int32_t max_pages_per_seq,
+    const int32_t* cu_q, const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
+    int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t window,
+    float scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream,
+    void* attn_begin_event, void* attn_end_event) {
+  return forward_paged(q, k_new, v_new, k_cache, v_cache, num_pages, page_size, block_table,
+                       max_pages_per_seq, cu_q, ctx_len, mode, num_seqs, total_q, num_q_heads,
+                       num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
+                       stream, attn_begin_event, attn_end_event);
 }
 
 namespace {

@@ -19,6 +19,14 @@
 //                          TMEM and run the online softmax and the epilogue.
 //   combine_kernel<D>      merges the partials of cut tiles by their LSE.
 //
+// Paged KV cache (block-table indirection): K and V live in pools of pages of
+// P = 2^page_shift token rows, [num_pages * P, Hkv, D]; block_table[s, p] is
+// the physical page of positions p*P .. p*P+P-1 of sequence s.  The work-list
+// launch then also appends the query tokens' K/V rows into their pages (CTAs
+// 1.. of the launch) and checks every page-table entry the attention will
+// read; the loaders look up each slice's page and load it in boxes of
+// min(P, BN / C) rows.
+//
 // Rules (DiffusionGemma, agentlenshq page, "dual-mode operation", "dynamic
 // per-sequence causal attention", "symmetric sliding-window attention"): a
 // causal query at position i sees keys j <= i, a bidirectional one every key of
@@ -56,7 +64,7 @@ constexpr int kErrTimeout = 5;
 struct TileDesc {
   int32_t q_row0;    // global query row of the tile's first token
   int32_t n_tok;     // query tokens in the tile (1 .. TT; 0 = no tile for this cluster rank)
-  int32_t kv_row0;   // global K/V row of the sequence's first key
+  int32_t kv_row0;   // global K/V row of the sequence's first key (paged: its page-table row offset)
   int32_t pos0;      // absolute position of the tile's first token
   int32_t L;         // keys of the sequence (context + queries)
   int32_t kt_first;  // first KV tile of the group's range (units of BN keys, sequence-relative)
@@ -87,6 +95,10 @@ struct FwdParams {
   float* lse;
   int* status;
   int Hq, G, TT, window, C;
+  // paged KV cache: block_table [B, bt_stride] (nullptr: contiguous K/V),
+  // pages of 2^page_shift rows, TMA boxes of page_box rows
+  const int32_t* block_table;
+  int page_shift, page_box;
   // >= 0: the K loader skips the TMA load of this (per-CTA) KV tile, so the
   // MMA warp's bounded wait for it expires (tests of the timeout path)
   int debug_skip_k_load;
@@ -138,14 +150,73 @@ __device__ void block_exclusive_scan(int64_t* data, int n) {
   __syncthreads();
 }
 
+// ------------------------------------------------ paged cache: the append
+struct PagedArgs {
+  const int32_t* block_table;    // [B, bt_stride]; nullptr: contiguous K/V
+  int bt_stride;                 // page-table entries per sequence
+  int page_shift;                // pages of 2^page_shift rows
+  int num_pages;
+  const __nv_bfloat16* k_new;    // [total_q, Hkv, D] or nullptr (no append)
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_cache;        // [num_pages << page_shift, Hkv, D]
+  __nv_bfloat16* v_cache;
+  int Hkv, D;
+};
+
+// Writes row r of k_new / v_new (query token t of sequence s) at position
+// ctx_len[s] + t of sequence s, 16 bytes per thread, grid-stride over the
+// CTAs 1 .. gridDim.x-1.  Every write is checked against the page table and
+// the pool; a bad entry records DG_ERR_INVALID_ARG and the row is skipped.
+__device__ void append_rows(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ ctx_len,
+                            int B, int total_q, const PagedArgs& pg, int* status) {
+  const int upr = pg.Hkv * pg.D / 8;  // 16-byte units per token row
+  const int64_t units = static_cast<int64_t>(total_q) * upr;
+  const int64_t step = static_cast<int64_t>(gridDim.x - 1) * blockDim.x;
+  const int P = 1 << pg.page_shift;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x; u < 2 * units;
+       u += step) {
+    const bool is_v = u >= units;
+    const int64_t uu = is_v ? u - units : u;
+    const int r = static_cast<int>(uu / upr);
+    const int c = static_cast<int>(uu - static_cast<int64_t>(r) * upr);
+    int lo = 0, hi = B - 1;  // sequence of row r: largest s with cu_q[s] <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu_q[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    const int t = r - cu_q[lo];
+    const int pos = ctx_len[lo] + t;
+    if (t < 0 || pos < 0 || (pos >> pg.page_shift) >= pg.bt_stride) {
+      record_error(status, kErrInvalid);
+      continue;
+    }
+    const int page = pg.block_table[static_cast<int64_t>(lo) * pg.bt_stride + (pos >> pg.page_shift)];
+    if (page < 0 || page >= pg.num_pages) {
+      record_error(status, kErrInvalid);
+      continue;
+    }
+    const int64_t row = (static_cast<int64_t>(page) << pg.page_shift) + (pos & (P - 1));
+    const uint4* src = reinterpret_cast<const uint4*>((is_v ? pg.v_new : pg.k_new) +
+                                                      static_cast<int64_t>(r) * pg.Hkv * pg.D) + c;
+    uint4* dst = reinterpret_cast<uint4*>((is_v ? pg.v_cache : pg.k_cache) + row * pg.Hkv * pg.D) + c;
+    *dst = __ldg(src);
+  }
+}
+
 // ------------------------------------------------------ work-list builder
+// CTA 0 builds the work list; with a paged cache, CTAs 1.. append the new K/V.
 __global__ void __launch_bounds__(1024, 1)
 build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ ctx_len,
                       const uint8_t* __restrict__ mode, int B, int total_q, int total_kv, int Hkv,
                       int TT, int BN, int window, int max_groups, int C, Workspace ws,
-                      int* status) {
+                      PagedArgs pg, int* status) {
+  if (blockIdx.x > 0) {
+    append_rows(cu_q, ctx_len, B, total_q, pg, status);
+    return;
+  }
   __shared__ int bad;
   const int tid = threadIdx.x;
+  const bool paged = pg.block_table != nullptr;
   if (tid == 0) bad = (cu_q[0] != 0 || cu_q[B] != total_q) ? 1 : 0;
   __syncthreads();
   for (int s = tid; s < B; s += 1024) {
@@ -159,10 +230,26 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     ws.seq_kv_off[s] = static_cast<int64_t>(c < 0 ? 0 : c) + nn;
   }
   __syncthreads();
+  if (paged && !bad) {
+    // every page the attention reads: pages 0 .. ceil(L / P) - 1 of each sequence
+    for (int s = 0; s < B; ++s) {
+      const int64_t L = static_cast<int64_t>(ctx_len[s]) + cu_q[s + 1] - cu_q[s];
+      const int64_t need = (L + (1 << pg.page_shift) - 1) >> pg.page_shift;
+      if (need > pg.bt_stride) {
+        if (tid == 0) bad = 1;
+        continue;
+      }
+      for (int64_t i = tid; i < need; i += 1024) {
+        const int page = pg.block_table[static_cast<int64_t>(s) * pg.bt_stride + i];
+        if (page < 0 || page >= pg.num_pages) atomicOr(&bad, 1);
+      }
+    }
+  }
+  __syncthreads();
   block_exclusive_scan(ws.seq_tile_off, B);
   block_exclusive_scan(ws.seq_kv_off, B);
   if (tid == 0) {
-    if (ws.seq_tile_off[B] > max_groups || ws.seq_kv_off[B] > total_kv) bad = 1;
+    if (ws.seq_tile_off[B] > max_groups || (!paged && ws.seq_kv_off[B] > total_kv)) bad = 1;
   }
   __syncthreads();
   if (bad) {
@@ -205,7 +292,7 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
       TileDesc td;
       td.q_row0 = cu_q[s] + t0;
       td.n_tok = present ? min(TT, n - t0) : 0;
-      td.kv_row0 = static_cast<int>(ws.seq_kv_off[s]);
+      td.kv_row0 = paged ? s * pg.bt_stride : static_cast<int>(ws.seq_kv_off[s]);
       td.pos0 = c + t0;
       td.L = L;
       td.kt_first = kv_lo / BN;
@@ -460,15 +547,37 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             continue;
           }
           mbar_arrive_expect_tx(full0 + 8u * stage, t_tx);
-          const int row = td.kv_row0 + (td.kt_first + j) * BN + rank * slice;
           const uint32_t dst = ring + stage * Cf::KV_BYTES + rank * slice * 128;
+          if (p.block_table == nullptr) {
+            const int row = td.kv_row0 + (td.kt_first + j) * BN + rank * slice;
 #pragma unroll
-          for (int kb = 0; kb < Cf::NKB; ++kb) {
-            if (C > 1)
-              tma_load_3d_multicast(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh,
-                                    row, cta_mask);
-            else
-              tma_load_3d(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh, row);
+            for (int kb = 0; kb < Cf::NKB; ++kb) {
+              if (C > 1)
+                tma_load_3d_multicast(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh,
+                                      row, cta_mask);
+              else
+                tma_load_3d(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh, row);
+            }
+          } else {
+            // positions past the sequence's last key read its last page
+            // (checked by the work-list launch); the softmax masks them
+            const int pos0 = (td.kt_first + j) * BN + rank * slice;
+            const int last_page = (td.L - 1) >> p.page_shift;
+            const int pmask = (1 << p.page_shift) - 1;
+            for (int r0 = 0; r0 < slice; r0 += p.page_box) {
+              const int pos = pos0 + r0;
+              const int page = __ldg(p.block_table + td.kv_row0 + min(pos >> p.page_shift, last_page));
+              const int row = (page << p.page_shift) + (pos & pmask);
+              const uint32_t d0 = dst + r0 * 128;
+#pragma unroll
+              for (int kb = 0; kb < Cf::NKB; ++kb) {
+                if (C > 1)
+                  tma_load_3d_multicast(d0 + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh,
+                                        row, cta_mask);
+                else
+                  tma_load_3d(d0 + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh, row);
+              }
+            }
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);

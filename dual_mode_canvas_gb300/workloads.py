@@ -176,3 +176,36 @@ def make_logits(wl: LogitsWorkload, device="cpu", dtype=torch.bfloat16):
     for n in wl.canvases:
         cu.append(cu[-1] + n)
     return x.to(dtype), torch.tensor(cu, dtype=torch.int32)
+
+
+# ------------------------------------------------------------ paged KV cache
+def make_paged_batch(wl: Workload, page_size: int, device="cpu", spare_pages: int = 7,
+                     dtype=torch.bfloat16):
+    """Inputs of ``wl`` over a paged KV cache.  Drawn from seed ``wl.seed``
+    in the order q, k_new, v_new (the query tokens' K/V, [total_q, Hkv, D]),
+    the whole K pool, the whole V pool ([num_pages, page_size, Hkv, D], every
+    row N(0, 1)), then a random permutation of the physical pages: sequence s
+    owns pages ``perm[o_s : o_s + ceil(L_s / page_size)]`` in order, and
+    ``spare_pages`` pages belong to no sequence.  Page-table entries past a
+    sequence's last page are -1.  The metadata (cu_q, ctx_len, mode,
+    block_table) stays on the host."""
+    gen = torch.Generator(device=device).manual_seed(wl.seed)
+    Hq, Hkv, D = wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    q = _randn(gen, (wl.total_q, Hq, D), device)
+    k_new = _randn(gen, (wl.total_q, Hkv, D), device)
+    v_new = _randn(gen, (wl.total_q, Hkv, D), device)
+    need = [-(-(c + n) // page_size) for c, n, _ in wl.seqs]
+    num_pages = sum(need) + spare_pages
+    k_cache = _randn(gen, (num_pages, page_size, Hkv, D), device)
+    v_cache = _randn(gen, (num_pages, page_size, Hkv, D), device)
+    perm = torch.randperm(num_pages, generator=gen, device=device).cpu()
+    table = torch.full((len(wl.seqs), max(need)), -1, dtype=torch.int32)
+    o = 0
+    for s, k in enumerate(need):
+        table[s, :k] = perm[o:o + k].to(torch.int32)
+        o += k
+    cu_q, ctx_len, mode = metadata(wl)
+    return dict(q=q.to(dtype), k_new=k_new.to(dtype), v_new=v_new.to(dtype),
+                k_cache=k_cache.to(dtype), v_cache=v_cache.to(dtype), block_table=table,
+                page_size=page_size, cu_q=cu_q, ctx_len=ctx_len, mode=mode, window=wl.window,
+                scale=wl.scale)

@@ -143,6 +143,61 @@ dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, const void* v,
                                     void* out, float* lse, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The same forward pass over a paged KV cache, with the append of the query
+ * tokens' K/V fused into the call.  DiffusionGemma pages: the encoder (causal)
+ * pass writes finished blocks into the KV cache and every committed canvas is
+ * appended to it (agentlenshq page, "dual-mode operation"; developer guide,
+ * "block autoregressive denoising", the prefill item); vLLM's prefix caching
+ * works unchanged, i.e. the cache is block-based (agentlenshq page,
+ * "dual-mode operation").  The pages do not describe the cache layout; this
+ * one is the common block-table layout:
+ *
+ *   k_cache, v_cache  bf16 device [num_pages, page_size, num_kv_heads, head_dim],
+ *                     16-byte aligned, caller-owned; the call writes the
+ *                     appended rows and reads the rest
+ *   page_size         rows per page: a power of two in [8, 65536];
+ *                     num_pages * page_size <= INT32_MAX
+ *   block_table       int32 device [num_seqs, max_pages_per_seq]:
+ *                     block_table[s][p] = physical page of positions
+ *                     p*page_size .. p*page_size+page_size-1 of sequence s;
+ *                     only entries 0 .. ceil((ctx_len[s]+n_s)/page_size)-1 are
+ *                     read, each must lie in [0, num_pages) (device-checked:
+ *                     DG_ERR_INVALID_ARG in the status word, nothing computed)
+ *   k_new, v_new      bf16 device [total_q, num_kv_heads, head_dim], packed like
+ *                     q: the K/V rows of the query tokens, written at positions
+ *                     ctx_len[s] .. ctx_len[s]+n_s-1 of their sequence before
+ *                     the attention reads the cache (this step's canvas
+ *                     overwrites the previous step's); both NULL when those
+ *                     rows are already in the cache.  The pages written must
+ *                     not be shared with another sequence of the batch.
+ *
+ * Everything else (q, cu_q, ctx_len, mode, shapes, window, scale, out, lse,
+ * status and ordering rules) is as for dg_attn_forward, and the workspace is
+ * dg_attn_workspace_size() bytes.  Keys of sequence s are positions
+ * 0 .. ctx_len[s]+n_s-1 read through its page-table row.
+ */
+dg_status_t dg_attn_forward_paged(const void* q, const void* k_new, const void* v_new,
+                                  void* k_cache, void* v_cache, int32_t num_pages,
+                                  int32_t page_size, const int32_t* block_table,
+                                  int32_t max_pages_per_seq, const int32_t* cu_q,
+                                  const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
+                                  int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t window, float scale, void* out,
+                                  float* lse, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/* dg_attn_forward_paged with two CUDA events (cudaEvent_t, created by the
+ * caller) recorded around the main attention kernel, as in
+ * dg_attn_forward_profiled. */
+dg_status_t dg_attn_forward_paged_profiled(
+    const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    int32_t num_pages, int32_t page_size, const int32_t* block_table, int32_t max_pages_per_seq,
+    const int32_t* cu_q, const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
+    int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t window,
+    float scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream,
+    void* attn_begin_event, void* attn_end_event);
+
+/* ---------------------------------------------------------------------------
  * Entropy-bounded acceptance of one denoise step (DiffusionGemma, agentlenshq
  * page, "sampling loop and entropy-bounded denoising"; 24-ai.news page, "the
  * mechanism for deciding finished tokens").  For every canvas position the
