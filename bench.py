@@ -216,10 +216,20 @@ def run_gpu(args):
     wl = wls.WORKLOADS[args.workload]
     binding.load_library()
     dev = torch.device("cuda")
-    batch = wls.make_batch(wl, device="cuda")
-    q, k, v = batch["q"], batch["k"], batch["v"]
+    paged = args.paged > 0
+    if paged:
+        # paged KV cache: the step's canvas K/V go in as k_new / v_new and the
+        # call appends them into their pages (inside the timed call)
+        batch = wls.make_paged_batch(wl, args.paged, device="cuda")
+        q, k, v = batch["q"], batch["k_new"], batch["v_new"]
+        k_cache, v_cache = batch["k_cache"], batch["v_cache"]
+        bt = batch["block_table"].cuda()
+        rows = [(0, wl.total_q)]  # k / v here are the new rows themselves
+    else:
+        batch = wls.make_batch(wl, device="cuda")
+        q, k, v = batch["q"], batch["k"], batch["v"]
+        rows = wls.canvas_rows(wl)
     cu_q, ctx, mode = batch["cu_q"].cuda(), batch["ctx_len"].cuda(), batch["mode"].cuda()
-    rows = wls.canvas_rows(wl)
     nsteps = args.warmup + args.steps
     loop = wl.steps > 1
     # canvases of every step, drawn up front (device) and mirrored in pinned host memory
@@ -253,6 +263,14 @@ def run_gpu(args):
                 o += b - a
         flush.fill_(s & 0xFF)
 
+    def call(events=None):
+        if paged:
+            binding.forward_paged(q, k, v, k_cache, v_cache, bt, cu_q, ctx, mode, wl.window, wl.scale,
+                                  out=out, lse=lse, workspace=ws, events=events)
+        else:
+            binding.forward(q, k, v, cu_q, ctx, mode, wl.window, wl.scale, out=out, lse=lse,
+                            workspace=ws, events=events)
+
     flops = algorithmic_flops(wl)
     nbytes = algorithmic_bytes(wl)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -263,8 +281,7 @@ def run_gpu(args):
             x.record(stream)
     for s in range(args.warmup):
         stage(s)
-        binding.forward(q, k, v, cu_q, ctx, mode, wl.window, wl.scale, out=out, lse=lse,
-                        workspace=ws)
+        call()
     torch.cuda.synchronize()
     st = binding.status()
     if st != binding.DG_OK:
@@ -278,8 +295,7 @@ def run_gpu(args):
             stage(s)
             e0, e1, a0, a1 = ev[s]
             e0.record(stream)
-            binding.forward(q, k, v, cu_q, ctx, mode, wl.window, wl.scale, out=out, lse=lse,
-                            workspace=ws, events=(a0, a1))
+            call(events=(a0, a1))
             e1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -316,8 +332,7 @@ def run_gpu(args):
                 k[a:b].copy_(kc_dev[o:o + b - a])
                 v[a:b].copy_(vc_dev[o:o + b - a])
                 o += b - a
-            binding.forward(q, k, v, cu_q, ctx, mode, wl.window, wl.scale, out=out, lse=lse,
-                            workspace=ws)
+            call()
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
             e1.record(stream)
@@ -348,7 +363,7 @@ def run_gpu(args):
         gbs = nbytes / (attn_avg_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(gbs / peaks["hbm_gbs"], 4)}
-    roof["traffic"] = NCU_TRAFFIC_BYTES.get(args.workload)
+    roof["traffic"] = None if paged else NCU_TRAFFIC_BYTES.get(args.workload)
     roof["peak_source"] = f"{peaks_src} ({'sustained' if (sustained and bound == 'tensor') else 'burst'})"
     roof["kernel"] = "fwd_kernel (persistent tcgen05 attention)"
     roof["kernel_ms_per_launch"] = round(attn_avg_ms, 4)
@@ -363,6 +378,8 @@ def run_gpu(args):
                    "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
                    "head_dim": wl.head_dim, "window": wl.window,
                    "l2": "flushed before every step (256 MiB write)",
+                   "kv_layout": (f"paged: {args.paged}-row pages, shuffled page table, canvas K/V "
+                                 "appended inside the timed call") if paged else "contiguous",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "denoise_steps_per_s": round(1000.0 / ms_per_step, 2),
         "algorithmic_gflop_per_step": round(flops / 1e9, 3),
@@ -502,6 +519,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--paged", type=int, default=0,
+                    help="page size: run the step through the paged KV cache (0: contiguous)")
     ap.add_argument("--workload", default="denoise_loop",
                     choices=sorted(wls.WORKLOADS) + sorted(wls.LOGITS_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
