@@ -513,6 +513,121 @@ def run_accept(args):
                      "peak_source": src, "kernel": "row_stats_kernel + accept_kernel"}}))
 
 
+def _a256(n):
+    return (n + 255) // 256 * 256
+
+
+def run_selfcond(args):
+    """The self-conditioning embedding average of one denoise step: softmax of
+    the LM-head logits times the token-embedding table (tensor-bound).  Value:
+    2 * rows * vocab * d_model / step time."""
+    world, rank, local = dist_setup()
+    wl = wls.SELFCOND_WORKLOADS[args.workload]
+    binding.load_library()
+    x, _ = wls.make_logits(wl.logits, device="cuda")
+    E = wls.make_embedding(wl.logits.vocab, wl.d_model, wl.seed, device="cuda")
+    rows, vocab, d = wl.logits.rows, wl.logits.vocab, wl.d_model
+    out = torch.empty((rows, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(binding.load_library().dg_selfcond_workspace_size(rows, vocab, d),
+                     dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    nsteps = args.warmup + args.steps
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(nsteps)]
+    for e in ev:
+        for y in e:
+            y.record(stream)
+    for s_ in range(args.warmup):
+        flush.fill_(s_ & 0xFF)
+        binding.self_conditioning(x, E, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        for s_ in range(args.warmup, nsteps):
+            flush.fill_(s_ & 0xFF)
+            e0, e1, a0, a1 = ev[s_]
+            e0.record(stream)
+            binding.self_conditioning(x, E, out=out, workspace=ws, events=(a0, a1))
+            e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    st = binding.status()
+    if st != binding.DG_OK:
+        raise RuntimeError(f"device status {st}")
+    ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.warmup, nsteps)]
+    kms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.warmup, nsteps)]
+    tot = max_over_ranks(world, float(sum(ms)))
+    kavg = max_over_ranks(world, float(np.mean(kms)))
+    flops = 2.0 * rows * vocab * d
+    nbytes = x.numel() * 2 + E.numel() * 2 + out.numel() * 4
+
+    # end to end: the step's logits host -> device, the result device -> host
+    hx = x.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_ms = []
+    for s_ in range(nsteps):
+        flush.fill_(s_ & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x.copy_(hx, non_blocking=True)
+        binding.self_conditioning(x, E, out=out, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if s_ >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_tot = max_over_ranks(world, float(sum(e2e_ms)))
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    sustained = tot > 1000.0
+    tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    tflops = world * flops * args.steps / (tot * 1e-3) / 1e12
+    ktf = flops / (kavg * 1e-3) / 1e12
+    t_tc = flops / (tc_peak * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    res = {
+        "metric": "self-conditioning embedding average TFLOP/s (softmax(logits) x E)",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded logits and N(0,1) embeddings, bf16)",
+        "config": {"workload": wl.name, "rows": rows, "vocab": vocab, "d_model": d,
+                   "l2": "flushed before every step (256 MiB write)"},
+        # row statistics, row constants, the GEMM, and the split sum when the
+        # workspace holds per-split partials (beyond the statistics)
+        "gpu_launches": (4 if ws.numel() > _a256(16 * rows * -(-(vocab + (7 if vocab % 8 else 0)) // 16384))
+                         + _a256(4 * rows) else 3) * args.steps * world,
+        "roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "achieved": round(ktf, 2),
+                     "peak": tc_peak, "unit": "TFLOP/s", "frac": round(ktf / tc_peak, 4),
+                     "traffic": None,
+                     "peak_source": f"{src} ({'sustained' if sustained else 'burst'})",
+                     "kernel": "sc_kernel (persistent tcgen05 softmax x E)",
+                     "kernel_ms_per_launch": round(kavg, 4),
+                     "tighter_roof_frac": round(max(t_tc, t_hbm) / (kavg * 1e-3), 4)},
+        "clocks": clk.summary(),
+        "e2e": {"value": round(world * flops * args.steps / (e2e_tot * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": x.numel() * 2,
+                "d2h_bytes_per_step": out.numel() * 4, "ms_per_step": round(e2e_tot / args.steps, 4)},
+    }
+    if not args.no_cpu_baseline:
+        import oracle.selfcond as sc
+        xr = x[:2].float().cpu().numpy().astype(np.float64)
+        Ec = E[:, :256].float().cpu().numpy().astype(np.float64)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < args.cpu_seconds and reps < 50:
+            sc.self_conditioning(xr, Ec)
+            reps += 1
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(2.0 * 2 * vocab * 256 * reps / dt / 1e12, 6),
+                               "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+                               "kind": "oracle",
+                               "sample": f"fp64 NumPy oracle, 2 rows x {vocab} vocabulary x 256 of {d} "
+                                         f"columns, {reps} repetition(s) in {dt:.1f} s"}
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,7 +637,8 @@ def main():
     ap.add_argument("--paged", type=int, default=0,
                     help="page size: run the step through the paged KV cache (0: contiguous)")
     ap.add_argument("--workload", default="denoise_loop",
-                    choices=sorted(wls.WORKLOADS) + sorted(wls.LOGITS_WORKLOADS))
+                    choices=sorted(wls.WORKLOADS) + sorted(wls.LOGITS_WORKLOADS) +
+                    sorted(wls.SELFCOND_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
@@ -532,6 +648,8 @@ def main():
         run_reference(args)
     elif args.workload in wls.LOGITS_WORKLOADS:
         run_accept(args)
+    elif args.workload in wls.SELFCOND_WORKLOADS:
+        run_selfcond(args)
     else:
         run_gpu(args)
 

@@ -28,6 +28,7 @@ DG_MODE_BIDIRECTIONAL = 1
 
 EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profiled",
             "dg_attn_forward_noalloc", "dg_attn_forward_paged", "dg_attn_forward_paged_profiled",
+            "dg_selfcond_workspace_size", "dg_selfcond_forward", "dg_selfcond_forward_profiled",
             "dg_accept_workspace_size", "dg_accept_step",
             "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
 
@@ -70,6 +71,12 @@ def load_library():
     lib.dg_attn_forward_paged.restype = ctypes.c_int
     lib.dg_attn_forward_paged_profiled.argtypes = lib.dg_attn_forward_paged.argtypes + [vp, vp]
     lib.dg_attn_forward_paged_profiled.restype = ctypes.c_int
+    lib.dg_selfcond_workspace_size.argtypes = [i32, i32, i32]
+    lib.dg_selfcond_workspace_size.restype = sz
+    lib.dg_selfcond_forward.argtypes = [vp, i32, i32, vp, i32, vp, vp, sz, vp]
+    lib.dg_selfcond_forward.restype = ctypes.c_int
+    lib.dg_selfcond_forward_profiled.argtypes = lib.dg_selfcond_forward.argtypes + [vp, vp]
+    lib.dg_selfcond_forward_profiled.restype = ctypes.c_int
     lib.dg_accept_workspace_size.argtypes = [i32, i32]
     lib.dg_accept_workspace_size.restype = sz
     f32 = ctypes.c_float
@@ -211,6 +218,39 @@ def forward_paged(q, k_new, v_new, k_cache, v_cache, block_table, cu_q, ctx_len,
     if rc != DG_OK:
         raise DgAttnError(rc, "dg_attn_forward_paged")
     return out, lse
+
+
+def self_conditioning(logits, embedding, *, out=None, workspace=None, stream=None, events=None):
+    """Probability-weighted embedding average through ``dg_selfcond_forward``.
+
+    logits [rows, vocab] bf16, embedding [vocab, d_model] bf16 (CUDA).  Returns
+    ``out`` [rows, d_model] fp32.  ``events=(begin, end)`` goes through
+    ``dg_selfcond_forward_profiled``: the events bracket the tensor-core kernel.
+    """
+    lib = load_library()
+    for name, t in (("logits", logits), ("embedding", embedding)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{name} must be a contiguous 2-D CUDA bfloat16 tensor")
+    rows, vocab = logits.shape
+    if embedding.shape[0] != vocab:
+        raise ValueError("embedding must be [vocab, d_model]")
+    d = embedding.shape[1]
+    if out is None:
+        out = torch.empty((rows, d), dtype=torch.float32, device=logits.device)
+    need = lib.dg_selfcond_workspace_size(rows, vocab, d)
+    if need == 0:
+        raise DgAttnError(DG_ERR_INVALID_ARG, "dg_selfcond_workspace_size")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=logits.device)
+    args = (_ptr(logits), rows, vocab, _ptr(embedding), d, _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if events is None:
+        rc = lib.dg_selfcond_forward(*args)
+    else:
+        rc = lib.dg_selfcond_forward_profiled(*args, events[0].cuda_event, events[1].cuda_event)
+    if rc != DG_OK:
+        raise DgAttnError(rc, "dg_selfcond_forward")
+    return out
 
 
 def accept_step(logits, cu_rows, accepted_in, argmax_prev, stable_in, entropy_budget: float,

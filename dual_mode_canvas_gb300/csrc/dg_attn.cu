@@ -14,6 +14,7 @@
 #include "dg_attn.h"
 #include "kernels.cuh"
 #include "acceptance.cuh"
+#include "selfcond.cuh"
 
 namespace dg {
 
@@ -38,6 +39,7 @@ struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
   int max_clusters[3][4] = {};  // [head_dim][cluster size]: co-resident clusters
+  int sc_max_clusters[2] = {};  // self-conditioning kernel, clusters of 1 / 2
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;   // device address of g_status
   void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
@@ -88,6 +90,31 @@ cudaError_t set_kernel_attrs(DeviceInfo& di) {
   return cudaSuccess;
 }
 
+cudaError_t set_sc_attrs(DeviceInfo& di) {
+  cudaError_t e = cudaFuncSetAttribute(sc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       ScCfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < 2; ++i) {
+    const int cs = i + 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs * (di.num_sms / cs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = ScCfg::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sc_kernel, &cfg) != cudaSuccess) n = 0;
+    di.sc_max_clusters[i] = n;
+  }
+  cudaGetLastError();
+  return cudaSuccess;
+}
+
 // One-time per-device setup (SM count, architecture, kernel attributes,
 // status word address).  Returns DG_OK or an error code.
 dg_status_t device_info(DeviceInfo** out) {
@@ -113,7 +140,7 @@ dg_status_t device_info(DeviceInfo** out) {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     if (set_kernel_attrs<64>(di) != cudaSuccess || set_kernel_attrs<128>(di) != cudaSuccess ||
-        set_kernel_attrs<256>(di) != cudaSuccess)
+        set_kernel_attrs<256>(di) != cudaSuccess || set_sc_attrs(di) != cudaSuccess)
       return DG_ERR_CUDA;
     void* sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status) != cudaSuccess) return DG_ERR_CUDA;
@@ -463,6 +490,153 @@ int stat_chunks(int32_t vocab) {
   return static_cast<int>((span + kStatChunk - 1) / kStatChunk);
 }
 }  // namespace
+
+namespace {
+int stat_chunks(int32_t vocab);
+
+// Self-conditioning plan: tiles, cluster size, vocabulary splits and the
+// workspace layout.  The split count depends only on the shapes and the SM
+// count, so the size query and the call agree.
+struct ScPlan {
+  int C, m_tiles, n_tiles, m_groups, splits, kblocks, chunks;
+  size_t off_stats, off_rowc, off_part, total;
+};
+
+ScPlan sc_plan(int rows, int vocab, int d, int num_sms) {
+  ScPlan pl;
+  pl.m_tiles = (rows + kRows - 1) / kRows;
+  pl.C = pl.m_tiles >= 2 ? 2 : 1;
+  pl.m_groups = (pl.m_tiles + pl.C - 1) / pl.C;
+  pl.n_tiles = (d + kScN - 1) / kScN;
+  pl.kblocks = (vocab + kScK - 1) / kScK;
+  pl.chunks = stat_chunks(vocab);
+  // split the vocabulary so the units spread evenly over the clusters:
+  // minimise ceil(units / clusters) / splits (the time of the busiest
+  // cluster), keeping at least 8 blocks per split
+  const int64_t per_split = static_cast<int64_t>(pl.m_groups) * pl.n_tiles;
+  const int clusters = std::max(1, num_sms / pl.C);
+  const int smax = std::max(1, std::min(64, pl.kblocks / 8));
+  pl.splits = 1;
+  double best = 1e30;
+  for (int S = 1; S <= smax; ++S) {
+    const double cost = static_cast<double>((per_split * S + clusters - 1) / clusters) / S;
+    if (cost < best - 1e-12) {
+      best = cost;
+      pl.splits = S;
+    }
+  }
+  size_t off = 0;
+  pl.off_stats = off;
+  off = align256(off + sizeof(RowPartial) * static_cast<size_t>(rows) * pl.chunks);
+  pl.off_rowc = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(rows));
+  pl.off_part = off;
+  if (pl.splits > 1)
+    off = align256(off + sizeof(float) * static_cast<size_t>(pl.splits) * pl.m_tiles * kRows *
+                             static_cast<size_t>(pl.n_tiles) * kScN);
+  pl.total = off;
+  return pl;
+}
+
+bool sc_shapes_ok(int32_t rows, int32_t vocab, int32_t d) {
+  return rows >= 1 && vocab >= 8 && vocab % 8 == 0 && d >= 8 && d % 8 == 0;
+}
+
+dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const void* embedding,
+                          int32_t d_model, float* out, void* workspace, size_t workspace_bytes,
+                          void* stream_ptr, void* ev_begin, void* ev_end) {
+  if (!sc_shapes_ok(rows, vocab, d_model)) return DG_ERR_INVALID_ARG;
+  if (!logits || !embedding || !out || !aligned(logits, 16) || !aligned(embedding, 16) ||
+      !aligned(out, 16))
+    return DG_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  const dg_status_t st = device_info(&di);
+  if (st != DG_OK) return st;
+  const ScPlan pl = sc_plan(rows, vocab, d_model, di->num_sms);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.total) return DG_ERR_WORKSPACE;
+  int ncl = di->sc_max_clusters[pl.C - 1];
+  if (ncl < 1) return DG_ERR_CUDA;
+  const int64_t units = static_cast<int64_t>(pl.splits) * pl.m_groups * pl.n_tiles;
+  if (units < ncl) ncl = static_cast<int>(units);
+
+  CUtensorMap ml, me;
+  // logits [rows, vocab]: boxes of 64 entries x 128 rows; E [vocab, d]: boxes
+  // of 64 columns x (64 / C) vocabulary rows
+  if (encode_map(&ml, logits, rows, 1, vocab, 1, kRows) != DG_OK ||
+      encode_map(&me, embedding, vocab, 1, d_model, 1, kScK / pl.C) != DG_OK)
+    return DG_ERR_INVALID_ARG;
+
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  RowPartial* stats = reinterpret_cast<RowPartial*>(w + pl.off_stats);
+  ScParams p;
+  p.rowc = reinterpret_cast<float*>(w + pl.off_rowc);
+  p.out = out;
+  p.part = pl.splits > 1 ? reinterpret_cast<float*>(w + pl.off_part) : nullptr;
+  p.status = di->status;
+  p.rows = rows;
+  p.vocab = vocab;
+  p.d = d_model;
+  p.m_tiles = pl.m_tiles;
+  p.n_tiles = pl.n_tiles;
+  p.m_groups = pl.m_groups;
+  p.splits = pl.splits;
+  p.kblocks = pl.kblocks;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  row_stats_kernel<<<static_cast<unsigned>(rows) * pl.chunks, kStatThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(logits), vocab, pl.chunks, stats);
+  sc_rowconst_kernel<<<(rows + 255) / 256, 256, 0, stream>>>(stats, rows, pl.chunks,
+                                                             const_cast<float*>(p.rowc));
+  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
+  if (e0 && cudaEventRecord(e0, stream) != cudaSuccess) return DG_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ncl * pl.C);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = ScCfg::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pl.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, sc_kernel, ml, me, p) != cudaSuccess) return DG_ERR_CUDA;
+  if (e1 && cudaEventRecord(e1, stream) != cudaSuccess) return DG_ERR_CUDA;
+  if (pl.splits > 1) {
+    const int64_t n4 = static_cast<int64_t>(rows) * (d_model / 4);
+    const int blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 8ll * di->num_sms));
+    sc_combine_kernel<<<blocks, 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  }
+  return DG_OK;
+}
+}  // namespace
+
+extern "C" size_t dg_selfcond_workspace_size(int32_t rows, int32_t vocab, int32_t d_model) {
+  if (!sc_shapes_ok(rows, vocab, d_model)) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sc_plan(rows, vocab, d_model, sms).total;
+}
+
+extern "C" dg_status_t dg_selfcond_forward(const void* logits, int32_t rows, int32_t vocab,
+                                           const void* embedding, int32_t d_model, float* out,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  return selfcond_impl(logits, rows, vocab, embedding, d_model, out, workspace, workspace_bytes,
+                       stream, nullptr, nullptr);
+}
+
+extern "C" dg_status_t dg_selfcond_forward_profiled(const void* logits, int32_t rows,
+                                                    int32_t vocab, const void* embedding,
+                                                    int32_t d_model, float* out, void* workspace,
+                                                    size_t workspace_bytes, void* stream,
+                                                    void* gemm_begin_event, void* gemm_end_event) {
+  return selfcond_impl(logits, rows, vocab, embedding, d_model, out, workspace, workspace_bytes,
+                       stream, gemm_begin_event, gemm_end_event);
+}
 
 extern "C" size_t dg_accept_workspace_size(int32_t rows, int32_t vocab) {
   if (rows < 0 || vocab < 1) return 0;

@@ -1,0 +1,375 @@
+// Self-conditioning input of a denoise step (DiffusionGemma, agentlenshq page,
+// "self-conditioning for stability"; 24-ai.news page, the self-conditioning
+// signal between iterations): the probability-weighted average of the token
+// embeddings under the previous step's softmax,
+//
+//   Y[r, :] = sum_v p[r, v] E[v, :],   p[r, :] = softmax(logits[r, :]).
+//
+//   row_stats_kernel (acceptance.cuh) then sc_rowconst_kernel: per row the
+//       constant c_r = m_r log2(e) + log2(s_r) of its softmax, so that
+//       p = 2^(x log2(e) - c_r) needs one FMA and one ex2 per logit.
+//   sc_kernel: a persistent tcgen05 GEMM.  Work units are (vocabulary split,
+//       group of C row tiles, 256-column tile of E); clusters take units
+//       round-robin with the split outermost, so the clusters running at any
+//       moment read the same vocabulary range of logits and E and share it
+//       in L2.  Per 64-entry vocabulary block: TMA brings the 128 x 64 logits
+//       tile of this CTA's rows and 1/C of the 64 x 256 E tile (multicast to
+//       the cluster); warps 0-3 (one row each) turn the logits into bf16
+//       probabilities written straight to TMEM; the MMA warp accumulates
+//       P (A from TMEM) x E (B, N-major in shared memory) into TMEM.
+//   sc_combine_kernel: sums the splits' fp32 partials when there are several.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "acceptance.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace dg {
+
+constexpr int kScN = 256;   // embedding columns per tile (UMMA N)
+constexpr int kScK = 64;    // vocabulary entries per block (one 128-byte row of bf16)
+constexpr int kScNL = 4;    // logits ring stages
+constexpr int kScNE = 4;    // embedding ring stages
+constexpr int kScNP = 4;    // probability buffers in TMEM
+
+struct ScCfg {
+  static constexpr int L_BYTES = kRows * kScK * 2;   // one logits tile, 16 KB
+  static constexpr int E_BYTES = kScK * kScN * 2;    // one embedding tile, 32 KB
+  static constexpr int OFF_L = 0;
+  static constexpr int OFF_E = OFF_L + kScNL * L_BYTES;
+  static constexpr int OFF_BAR = OFF_E + kScNE * E_BYTES;
+  static constexpr int B_L_FULL = 0, B_L_EMPTY = kScNL, B_E_FULL = 2 * kScNL,
+                       B_E_EMPTY = 2 * kScNL + kScNE, B_P_FULL = 2 * kScNL + 2 * kScNE,
+                       B_P_EMPTY = B_P_FULL + kScNP, B_ACC_FULL = B_P_EMPTY + kScNP,
+                       B_ACC_EMPTY = B_ACC_FULL + 1, B_DRAIN = B_ACC_EMPTY + 1,
+                       NUM_BARS = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // slack for 1024-byte alignment
+  // TMEM: the fp32 accumulator (kScN columns), then kScNP probability buffers
+  // of kScK / 2 columns (packed bf16 pairs)
+  static constexpr uint32_t TM_ACC = 0, TM_P = kScN;
+  static_assert(kScN + kScNP * (kScK / 2) <= static_cast<int>(kTmemCols), "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct ScParams {
+  const float* rowc;  // [rows] c_r
+  float* out;         // [rows, d] fp32, written directly when splits == 1
+  float* part;        // [splits, m_tiles * 128, n_tiles * kScN] fp32 when splits > 1
+  int* status;
+  int rows, vocab, d;
+  int m_tiles, n_tiles, m_groups, splits, kblocks;
+};
+
+struct ScUnit {
+  int split, mt, nt, kb0, kb1;
+};
+
+// Unit u: split outermost, then the group of C row tiles, then the E tile.
+__device__ __forceinline__ ScUnit sc_unit(const ScParams& p, int64_t u, int C, int rank) {
+  const int64_t per_split = static_cast<int64_t>(p.m_groups) * p.n_tiles;
+  ScUnit w;
+  w.split = static_cast<int>(u / per_split);
+  const int rem = static_cast<int>(u - w.split * per_split);
+  const int mg = rem / p.n_tiles;
+  w.nt = rem - mg * p.n_tiles;
+  w.mt = mg * C + rank;
+  w.kb0 = static_cast<int>(static_cast<int64_t>(w.split) * p.kblocks / p.splits);
+  w.kb1 = static_cast<int>(static_cast<int64_t>(w.split + 1) * p.kblocks / p.splits);
+  return w;
+}
+
+// One thread per row: merge the row's chunk statistics in order and write
+// c_r = m log2(e) + log2(s).
+__global__ void sc_rowconst_kernel(const RowPartial* __restrict__ part, int rows, int chunks,
+                                   float* __restrict__ rowc) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  float m = -INFINITY, s = 0.f, t = 0.f;
+  int a = INT32_MAX;
+  for (int c = 0; c < chunks; ++c) {
+    const RowPartial q = part[static_cast<size_t>(r) * chunks + c];
+    merge_stats(m, s, t, a, q.m, q.s, q.t, q.arg);
+  }
+  rowc[r] = m * kLog2e + log2f(s);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUtensorMap tm_e,
+          const ScParams p) {
+  using Cf = ScCfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* sptr = smem_raw + (sbase - raw_base);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int C = static_cast<int>(cluster_size());
+  const int rank = static_cast<int>(cluster_cta_rank());
+  const int cl = static_cast<int>(cluster_index());
+  const int ncl = static_cast<int>(cluster_count());
+  const int64_t U = static_cast<int64_t>(p.splits) * p.m_groups * p.n_tiles;
+  const uint16_t cta_mask = static_cast<uint16_t>((1u << C) - 1u);
+
+  const uint32_t sL = sbase + Cf::OFF_L;
+  const uint32_t sE = sbase + Cf::OFF_E;
+  const uint32_t bars = sbase + Cf::OFF_BAR;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + Cf::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + Cf::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScNL; ++s) {
+      mbar_init(bar(Cf::B_L_FULL + s), 1);
+      mbar_init(bar(Cf::B_L_EMPTY + s), kRows);
+    }
+    // an E slot is free once every CTA of the cluster has consumed it
+    for (int s = 0; s < kScNE; ++s) {
+      mbar_init(bar(Cf::B_E_FULL + s), 1);
+      mbar_init(bar(Cf::B_E_EMPTY + s), C);
+    }
+    for (int s = 0; s < kScNP; ++s) {
+      mbar_init(bar(Cf::B_P_FULL + s), kRows);
+      mbar_init(bar(Cf::B_P_EMPTY + s), 1);
+    }
+    mbar_init(bar(Cf::B_ACC_FULL), 1);
+    mbar_init(bar(Cf::B_ACC_EMPTY), kRows);
+    mbar_init(bar(Cf::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tm_l);
+    tma_prefetch_desc(&tm_e);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (C > 1) cluster_sync_all();  // peers' barriers exist before any multicast
+
+  if (warp == kTmaWarp || warp == kVLoadWarp) {
+    // ----------------------------------------------------------- producers
+    // warp 4 loads this CTA's logits tiles, warp 6 its 1/C slice of every E
+    // tile, multicast to the cluster
+    if (lane == 0) {
+      const bool is_l = (warp == kTmaWarp);
+      const int NS = is_l ? kScNL : kScNE;
+      const uint32_t full0 = bar(is_l ? Cf::B_L_FULL : Cf::B_E_FULL);
+      const uint32_t empty0 = bar(is_l ? Cf::B_L_EMPTY : Cf::B_E_EMPTY);
+      const int slice = kScK / C;  // E rows this CTA loads
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      bool ok = true;
+      for (int64_t u = cl; ok && u < U; u += ncl) {
+        const ScUnit w = sc_unit(p, u, C, rank);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!wait_phase(empty0 + 8u * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (is_l) {
+            mbar_arrive_expect_tx(full0 + 8u * stage, Cf::L_BYTES);
+            tma_load_3d(sL + stage * Cf::L_BYTES, &tm_l, full0 + 8u * stage, kb * kScK, 0,
+                        w.mt * kRows);
+          } else {
+            mbar_arrive_expect_tx(full0 + 8u * stage, Cf::E_BYTES);  // all C slices
+            const uint32_t dst = sE + stage * Cf::E_BYTES + rank * slice * 128;
+#pragma unroll
+            for (int nb = 0; nb < kScN / 64; ++nb) {
+              if (C > 1)
+                tma_load_3d_multicast(dst + nb * (kScK * 128), &tm_e, full0 + 8u * stage,
+                                      w.nt * kScN + nb * 64, 0, kb * kScK + rank * slice, cta_mask);
+              else
+                tma_load_3d(dst + nb * (kScK * 128), &tm_e, full0 + 8u * stage,
+                            w.nt * kScN + nb * 64, 0, kb * kScK);
+            }
+          }
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == static_cast<uint32_t>(NS)) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // let loads already in flight land before the CTA's shared memory goes away
+        for (int st = 0; st < NS; ++st)
+          if (issued_mask & (1u << st)) drain_wait(full0 + 8u * st, (issued_phase >> st) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    // ACC += P (128 x 64, bf16 in TMEM) x E (64 x 256, N-major in shared
+    // memory), four K=16 steps per vocabulary block; one elected lane issues
+    constexpr uint32_t idesc = idesc_bf16_f32(kRows, kScN, 0, 1);
+    uint32_t e_stage = 0, e_phase = 0, g = 0, ui = 0;
+    bool ok = true;
+    for (int64_t u = cl; ok && u < U; u += ncl, ++ui) {
+      const ScUnit w = sc_unit(p, u, C, rank);
+      // the accumulator is free once the previous unit's epilogue has read it
+      if (ui > 0 &&
+          !__all_sync(0xffffffffu, wait_phase(bar(Cf::B_ACC_EMPTY), (ui - 1) & 1, abort_flag, p.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+        const uint32_t ps = g % kScNP, pph = (g / kScNP) & 1;
+        if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_P_FULL + ps), pph, abort_flag, p.status) &&
+                                         wait_phase(bar(Cf::B_E_FULL + e_stage), e_phase, abort_flag, p.status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t e_base = sE + e_stage * Cf::E_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < kScK / 16; ++kk) {
+          const uint64_t b = smem_desc_sw128(e_base + kk * 2048, kScK * 128, 1024);
+          umma_bf16_ts_warp(tmem + Cf::TM_ACC, tmem + Cf::TM_P + ps * (kScK / 2) + kk * 8, b, idesc,
+                            (kb == w.kb0 && kk == 0) ? 0u : 1u);
+        }
+        umma_commit_warp(bar(Cf::B_P_EMPTY + ps));
+        if (C > 1) umma_commit_multicast_warp(bar(Cf::B_E_EMPTY + e_stage), cta_mask);
+        else umma_commit_warp(bar(Cf::B_E_EMPTY + e_stage));
+        if (++e_stage == kScNE) { e_stage = 0; e_phase ^= 1; }
+      }
+      if (!ok) break;
+      umma_commit_warp(bar(Cf::B_ACC_FULL));
+    }
+    // every MMA issued by this thread has finished before TMEM is released
+    umma_commit_warp(bar(Cf::B_DRAIN));
+    drain_wait(bar(Cf::B_DRAIN), 0);
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------ probabilities and epilogue (one row each)
+    const int r = threadIdx.x;  // row of the tile == TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint64_t l2e2 = f32x2(kLog2e, kLog2e);
+    uint32_t l_stage = 0, l_phase = 0, g = 0, ui = 0;
+    bool ok = true;
+    for (int64_t u = cl; ok && u < U; u += ncl, ++ui) {
+      const ScUnit w = sc_unit(p, u, C, rank);
+      const int row = w.mt * kRows + r;
+      const bool row_ok = row < p.rows;
+      // rows past the end (zero-filled by TMA) get p = 2^-inf = 0
+      const float c = row_ok ? p.rowc[row] : INFINITY;
+      const uint64_t nc2 = f32x2(-c, -c);
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+        if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_L_FULL + l_stage), l_phase, abort_flag, p.status))) {
+          ok = false;
+          break;
+        }
+        // this row's 128 bytes; 16-byte chunk j sits at chunk j ^ (row & 7)
+        uint32_t x[kScK / 2];
+        const uint32_t rb = sL + l_stage * Cf::L_BYTES + r * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t a = rb + ((static_cast<uint32_t>(j) ^ (r & 7)) << 4);
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x[4 * j]), "=r"(x[4 * j + 1]), "=r"(x[4 * j + 2]), "=r"(x[4 * j + 3])
+                       : "r"(a));
+        }
+        mbar_arrive(bar(Cf::B_L_EMPTY + l_stage));
+        if (++l_stage == kScNL) { l_stage = 0; l_phase ^= 1; }
+        // p = 2^(x log2(e) - c_r), two logits per fp32x2 FMA
+        uint32_t pk[kScK / 2];
+#pragma unroll
+        for (int i = 0; i < kScK / 2; ++i) {
+          float t0, t1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(x[i] << 16), __uint_as_float(x[i] & 0xFFFF0000u)),
+                                l2e2, nc2),
+                      t0, t1);
+          pk[i] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
+        }
+        if ((kb + 1) * kScK > p.vocab) {
+          // the block past the vocabulary: those entries (zero-filled by TMA) get p = 0
+#pragma unroll
+          for (int i = 0; i < kScK / 2; ++i) {
+            const int v0 = kb * kScK + 2 * i;
+            if (v0 >= p.vocab) pk[i] = 0u;
+            else if (v0 + 1 >= p.vocab) pk[i] &= 0xFFFFu;
+          }
+        }
+        const uint32_t ps = g % kScNP, pph = (g / kScNP) & 1;
+        if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_P_EMPTY + ps), pph ^ 1, abort_flag, p.status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st32(lane_base + Cf::TM_P + ps * (kScK / 2), pk);
+        tc_fence_before();
+        mbar_arrive(bar(Cf::B_P_FULL + ps));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_ACC_FULL), ui & 1, abort_flag, p.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int col0 = w.nt * kScN;
+      float* dst = p.splits == 1
+                       ? p.out + static_cast<size_t>(row) * p.d + col0
+                       : p.part + (static_cast<size_t>(w.split) * p.m_tiles * kRows + row) *
+                                      (static_cast<size_t>(p.n_tiles) * kScN) + col0;
+      const bool direct = p.splits == 1;
+#pragma unroll 1
+      for (int cc = 0; cc < kScN / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + Cf::TM_ACC + cc * 32, o);
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int col = cc * 32 + 4 * e;
+            if (!direct || col0 + col < p.d)
+              *reinterpret_cast<float4*>(dst + col) =
+                  make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                              __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(Cf::B_ACC_EMPTY));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  // no CTA leaves while a peer may still multicast into its shared memory
+  if (C > 1) cluster_sync_all();
+}
+
+// out[r, c] = sum over splits of part[split, r, c], four columns per thread.
+__global__ void sc_combine_kernel(const ScParams p) {
+  const int d4 = p.d / 4;
+  const size_t ld = static_cast<size_t>(p.n_tiles) * kScN;
+  const size_t split_stride = static_cast<size_t>(p.m_tiles) * kRows * ld;
+  const int64_t total = static_cast<int64_t>(p.rows) * d4;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / d4);
+    const int c = static_cast<int>(i - static_cast<int64_t>(r) * d4) * 4;
+    const float* src = p.part + static_cast<size_t>(r) * ld + c;
+    float4 acc = *reinterpret_cast<const float4*>(src);
+    for (int s = 1; s < p.splits; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(src + s * split_stride);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(p.out + static_cast<size_t>(r) * p.d + c) = acc;
+  }
+}
+
+}  // namespace dg

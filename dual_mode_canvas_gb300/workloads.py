@@ -209,3 +209,29 @@ def make_paged_batch(wl: Workload, page_size: int, device="cpu", spare_pages: in
                 k_cache=k_cache.to(dtype), v_cache=v_cache.to(dtype), block_table=table,
                 page_size=page_size, cu_q=cu_q, ctx_len=ctx_len, mode=mode, window=wl.window,
                 scale=wl.scale)
+
+
+# ------------------------------------------------------------ self-conditioning
+@dataclass(frozen=True)
+class SelfCondWorkload:
+    """LM-head logits of one denoise step and the token-embedding table."""
+    name: str
+    logits: LogitsWorkload
+    d_model: int
+    seed: int
+
+
+# The pages give neither the model width nor the vocabulary size: d_model 2560
+# and the 262144-token vocabulary of the acceptance workload are assumptions.
+SELFCOND_WORKLOADS = {
+    "selfcond_small": SelfCondWorkload("selfcond_small", LogitsWorkload("sc_small", (256, 44), 5000, 30),
+                                       320, 31),
+    "selfcond_step": SelfCondWorkload("selfcond_step", LOGITS_WORKLOADS["accept_step"], 2560, 32),
+}
+
+
+def make_embedding(vocab: int, d_model: int, seed: int, device="cpu", dtype=torch.bfloat16):
+    """Token-embedding table [vocab, d_model]: N(0, 1) from ``seed``, rounded to
+    ``dtype``."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    return _randn(gen, (vocab, d_model), device).to(dtype)

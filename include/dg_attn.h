@@ -198,6 +198,45 @@ dg_status_t dg_attn_forward_paged_profiled(
     void* attn_begin_event, void* attn_end_event);
 
 /* ---------------------------------------------------------------------------
+ * Self-conditioning input of the next denoise step (DiffusionGemma, agentlenshq
+ * page, "self-conditioning for stability"; 24-ai.news page, the
+ * self-conditioning signal between iterations): every canvas position's
+ * softmax distribution over the vocabulary becomes the probability-weighted
+ * average of the token embeddings,
+ *
+ *   out[r, :] = sum_v softmax(logits[r, :])_v * embedding[v, :]
+ *
+ * (softmax at temperature 1; the gated MLP the model applies afterwards is not
+ * part of this call).  The probabilities are rounded to bf16 for the tensor
+ * cores; sums are fp32.
+ *
+ *   logits     bf16 device [rows, vocab], row-major, 16-byte aligned;
+ *              vocab % 8 == 0; -inf entries are masked tokens, NaN is not
+ *              allowed; a row needs at least one finite logit
+ *   embedding  bf16 device [vocab, d_model], row-major, 16-byte aligned;
+ *              d_model % 8 == 0
+ *   out        fp32 device [rows, d_model], 16-byte aligned, caller-owned
+ *   workspace  >= dg_selfcond_workspace_size(rows, vocab, d_model) bytes,
+ *              256-byte aligned (row statistics and, for large vocabularies,
+ *              per-split fp32 partial sums)
+ *
+ * Asynchronous on `stream`; no allocation; host-checkable errors return
+ * immediately (DG_ERR_INVALID_ARG, DG_ERR_WORKSPACE).
+ */
+size_t dg_selfcond_workspace_size(int32_t rows, int32_t vocab, int32_t d_model);
+
+dg_status_t dg_selfcond_forward(const void* logits, int32_t rows, int32_t vocab,
+                                const void* embedding, int32_t d_model, float* out,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* dg_selfcond_forward with two CUDA events (cudaEvent_t, created by the caller)
+ * recorded around its tensor-core kernel. */
+dg_status_t dg_selfcond_forward_profiled(const void* logits, int32_t rows, int32_t vocab,
+                                         const void* embedding, int32_t d_model, float* out,
+                                         void* workspace, size_t workspace_bytes, void* stream,
+                                         void* gemm_begin_event, void* gemm_end_event);
+
+/* ---------------------------------------------------------------------------
  * Entropy-bounded acceptance of one denoise step (DiffusionGemma, agentlenshq
  * page, "sampling loop and entropy-bounded denoising"; 24-ai.news page, "the
  * mechanism for deciding finished tokens").  For every canvas position the
