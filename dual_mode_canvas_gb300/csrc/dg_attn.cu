@@ -605,9 +605,8 @@ dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const
   if (cudaLaunchKernelEx(&cfg, sc_kernel, ml, me, p) != cudaSuccess) return DG_ERR_CUDA;
   if (e1 && cudaEventRecord(e1, stream) != cudaSuccess) return DG_ERR_CUDA;
   if (pl.splits > 1) {
-    const int64_t n4 = static_cast<int64_t>(rows) * (d_model / 4);
-    const int blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 8ll * di->num_sms));
-    sc_combine_kernel<<<blocks, 256, 0, stream>>>(p);
+    const dim3 grid((rows + 31) / 32, (d_model + 31) / 32);
+    sc_combine_kernel<<<grid, dim3(32, 8), 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   }
   return DG_OK;

@@ -31,8 +31,8 @@ namespace dg {
 
 constexpr int kScN = 256;   // embedding columns per tile (UMMA N)
 constexpr int kScK = 64;    // vocabulary entries per block (one 128-byte row of bf16)
-constexpr int kScNL = 4;    // logits ring stages
-constexpr int kScNE = 4;    // embedding ring stages
+constexpr int kScNL = 3;    // logits ring stages (read into registers at once)
+constexpr int kScNE = 5;    // embedding ring stages (held until the MMA is done)
 constexpr int kScNP = 4;    // probability buffers in TMEM
 
 struct ScCfg {
@@ -58,7 +58,8 @@ struct ScCfg {
 struct ScParams {
   const float* rowc;  // [rows] c_r
   float* out;         // [rows, d] fp32, written directly when splits == 1
-  float* part;        // [splits, m_tiles * 128, n_tiles * kScN] fp32 when splits > 1
+  float* part;        // splits > 1: fp32 [splits, m_tiles, n_tiles, kScN, 128], each
+                      // tile column-major so the epilogue's stores coalesce
   int* status;
   int rows, vocab, d;
   int m_tiles, n_tiles, m_groups, splits, kblocks;
@@ -313,26 +314,42 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
         break;
       }
       tc_fence_after();
-      const int col0 = w.nt * kScN;
-      float* dst = p.splits == 1
-                       ? p.out + static_cast<size_t>(row) * p.d + col0
-                       : p.part + (static_cast<size_t>(w.split) * p.m_tiles * kRows + row) *
-                                      (static_cast<size_t>(p.n_tiles) * kScN) + col0;
-      const bool direct = p.splits == 1;
+      if (p.splits == 1) {
+        // one split: this row straight into out (small problems only)
+        const int col0 = w.nt * kScN;
+        float* dst = p.out + static_cast<size_t>(row) * p.d + col0;
 #pragma unroll 1
-      for (int cc = 0; cc < kScN / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + Cf::TM_ACC + cc * 32, o);
-        if (row_ok) {
+        for (int cc = 0; cc < kScN / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + Cf::TM_ACC + cc * 32, o);
+          if (row_ok) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int col = cc * 32 + 4 * e;
-            if (!direct || col0 + col < p.d)
-              *reinterpret_cast<float4*>(dst + col) =
-                  make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                              __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+            for (int e = 0; e < 8; ++e) {
+              const int col = cc * 32 + 4 * e;
+              if (col0 + col < p.d)
+                *reinterpret_cast<float4*>(dst + col) =
+                    make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+            }
           }
         }
+      } else if (w.mt < p.m_tiles) {
+        // column-major partial tile: for each column the warp writes 32
+        // consecutive rows (128 bytes)
+        float* dst = p.part + ((static_cast<size_t>(w.split) * p.m_tiles + w.mt) * p.n_tiles + w.nt) *
+                                  (static_cast<size_t>(kScN) * kRows) + r;
+#pragma unroll 1
+        for (int cc = 0; cc < kScN / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + Cf::TM_ACC + cc * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dst[static_cast<size_t>(cc * 32 + e) * kRows] = __uint_as_float(o[e]);
+        }
+      } else {
+        // a cluster rank past the last row tile: nothing to write, but the
+        // accumulator is read like the others' before it is released
+        uint32_t o[32];
+        tmem_ld32(lane_base + Cf::TM_ACC, o);
       }
       tc_fence_before();
       mbar_arrive(bar(Cf::B_ACC_EMPTY));
@@ -349,26 +366,34 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
   if (C > 1) cluster_sync_all();
 }
 
-// out[r, c] = sum over splits of part[split, r, c], four columns per thread.
-__global__ void sc_combine_kernel(const ScParams p) {
-  const int d4 = p.d / 4;
-  const size_t ld = static_cast<size_t>(p.n_tiles) * kScN;
-  const size_t split_stride = static_cast<size_t>(p.m_tiles) * kRows * ld;
-  const int64_t total = static_cast<int64_t>(p.rows) * d4;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(i / d4);
-    const int c = static_cast<int>(i - static_cast<int64_t>(r) * d4) * 4;
-    const float* src = p.part + static_cast<size_t>(r) * ld + c;
-    float4 acc = *reinterpret_cast<const float4*>(src);
-    for (int s = 1; s < p.splits; ++s) {
-      const float4 v = *reinterpret_cast<const float4*>(src + s * split_stride);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+// out[r, c] = sum over splits of the partial tiles: a 32 x 32 block of out
+// per CTA, read along rows (the tiles are column-major), written along
+// columns through a shared-memory transpose.
+__global__ void __launch_bounds__(256) sc_combine_kernel(const ScParams p) {
+  __shared__ float t[32][33];
+  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
+  const int r = r0 + tx;
+  const int mt = r / kRows, rl = r - mt * kRows;
+  const size_t tile = static_cast<size_t>(kScN) * kRows;
+  const size_t split_stride = static_cast<size_t>(p.m_tiles) * p.n_tiles * tile;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = c0 + ty + 8 * k;
+    float acc = 0.f;
+    if (r < p.rows && c < p.d) {
+      const int nt = c / kScN, cl = c - nt * kScN;
+      const float* src = p.part + (static_cast<size_t>(mt) * p.n_tiles + nt) * tile +
+                         static_cast<size_t>(cl) * kRows + rl;
+      for (int s = 0; s < p.splits; ++s) acc += src[s * split_stride];
     }
-    *reinterpret_cast<float4*>(p.out + static_cast<size_t>(r) * p.d + c) = acc;
+    t[ty + 8 * k][tx] = acc;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int rr = r0 + ty + 8 * k, cc = c0 + tx;
+    if (rr < p.rows && cc < p.d) p.out[static_cast<size_t>(rr) * p.d + cc] = t[tx][ty + 8 * k];
   }
 }
 

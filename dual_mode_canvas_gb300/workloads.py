@@ -227,6 +227,10 @@ SELFCOND_WORKLOADS = {
     "selfcond_small": SelfCondWorkload("selfcond_small", LogitsWorkload("sc_small", (256, 44), 5000, 30),
                                        320, 31),
     "selfcond_step": SelfCondWorkload("selfcond_step", LOGITS_WORKLOADS["accept_step"], 2560, 32),
+    # the same step over a quarter of the vocabulary: a profiling-sized case
+    # (about 0.5 GB on the device, still larger than L2)
+    "selfcond_v64k": SelfCondWorkload("selfcond_v64k",
+                                      LogitsWorkload("v64k", (256, 256, 256, 256), 65536, 33), 2560, 34),
 }
 
 
