@@ -484,23 +484,65 @@ def run_accept(args):
     nsteps = args.warmup + args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(nsteps)]
-    for s_ in range(nsteps):
+    stream = torch.cuda.current_stream()
+    for s_ in range(args.warmup):
         flush.fill_(s_ & 0xFF)
         binding.accept_step(x, cu, acc_in, prev, stable, 2.0, 3.0, 3, s_, 48, workspace=ws,
                             events=ev[s_])
     torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        for s_ in range(args.warmup, nsteps):
+            flush.fill_(s_ & 0xFF)
+            binding.accept_step(x, cu, acc_in, prev, stable, 2.0, 3.0, 3, s_, 48, workspace=ws,
+                                events=ev[s_])
+        torch.cuda.synchronize()
+    barrier(world)
     st = binding.status()
     if st != binding.DG_OK:
         raise RuntimeError(f"device status {st}")
     ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.warmup, nsteps)]
-    tot = replicas.aggregate(float(sum(ms)), 0.0, device="cuda")[0]
+    tot = max_over_ranks(world, float(sum(ms)))
     nbytes = x.numel() * 2 + rows * (4 + 4 + 4 + 1 + 1 + 4)
+
+    # end to end: the step's logits host -> device, the per-row results and
+    # per-canvas flags device -> host
+    hx = x.cpu().pin_memory()
+    e2e_ms = []
+    res_h = None
+    for s_ in range(nsteps):
+        flush.fill_(s_ & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x.copy_(hx, non_blocking=True)
+        res = binding.accept_step(x, cu, acc_in, prev, stable, 2.0, 3.0, 3, s_, 48, workspace=ws)
+        res_h = {k: v.to("cpu", non_blocking=True) for k, v in res.items()}
+        e1.record(stream)
+        e1.synchronize()
+        if s_ >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_tot = max_over_ranks(world, float(sum(e2e_ms)))
+    d2h = sum(v.numel() * v.element_size() for v in res_h.values())
     if rank != 0:
         return
     peaks, src = load_peaks()
     gbs = world * nbytes * args.steps / (tot * 1e-3) / 1e9
     kgbs = nbytes / (float(np.mean(ms)) * 1e-3) / 1e9
-    print(json.dumps({
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle.acceptance as oacc
+        sample = x[:8].float().cpu().numpy()
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < args.cpu_seconds and reps < 50:
+            oacc.row_stats(sample)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(sample.size * 2 * reps / dt / 1e9, 3), "unit": "GB/s",
+               "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"fp64 NumPy oracle row statistics of 8 of {rows} rows x {wl.vocab} "
+                         f"logits, {reps} repetition(s) in {dt:.1f} s (bf16 bytes counted)"}
+    line = {
         "metric": "entropy-bounded acceptance step GB/s (logits read once)", "value": round(gbs, 1),
         "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot / args.steps, 4), "higher_is_better": True, "scaling": "weak",
@@ -510,7 +552,14 @@ def run_accept(args):
         "gpu_launches": 2 * args.steps * world,
         "roofline": {"bound": "hbm", "achieved": round(kgbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(kgbs / peaks["hbm_gbs"], 4), "traffic": None,
-                     "peak_source": src, "kernel": "row_stats_kernel + accept_kernel"}}))
+                     "peak_source": src, "kernel": "row_stats_kernel + accept_kernel"},
+        "clocks": clk.summary(),
+        "e2e": {"value": round(world * nbytes * args.steps / (e2e_tot * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_tot / args.steps, 4)}}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line))
 
 
 def _a256(n):
