@@ -98,7 +98,7 @@ cudaError_t set_sc_attrs(DeviceInfo& di) {
     const int cs = i + 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs * (di.num_sms / cs));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kScThreads);
     cfg.dynamicSmemBytes = ScCfg::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -592,7 +592,7 @@ dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const
   if (e0 && cudaEventRecord(e0, stream) != cudaSuccess) return DG_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ncl * pl.C);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kScThreads);
   cfg.dynamicSmemBytes = ScCfg::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -14,7 +14,8 @@
 //       moment read the same vocabulary range of logits and E and share it
 //       in L2.  Per 64-entry vocabulary block: TMA brings the 128 x 64 logits
 //       tile of this CTA's rows and 1/C of the 64 x 256 E tile (multicast to
-//       the cluster); warps 0-3 (one row each) turn the logits into bf16
+//       the cluster); eight warps, two per TMEM lane quadrant (one row and
+//       half of the block's columns per thread), turn the logits into bf16
 //       probabilities written straight to TMEM; the MMA warp accumulates
 //       P (A from TMEM) x E (B, N-major in shared memory) into TMEM.
 //   sc_combine_kernel: sums the splits' fp32 partials when there are several.
@@ -34,6 +35,10 @@ constexpr int kScK = 64;    // vocabulary entries per block (one 128-byte row of
 constexpr int kScNL = 3;    // logits ring stages (read into registers at once)
 constexpr int kScNE = 5;    // embedding ring stages (held until the MMA is done)
 constexpr int kScNP = 4;    // probability buffers in TMEM
+// warps 0-3 and 7-10 compute probabilities (two per TMEM lane quadrant, each
+// half of a block's columns); warps 4 / 6 load, warp 5 issues MMAs
+constexpr int kScThreads = 352;
+constexpr int kScXform = 256;  // probability threads
 
 struct ScCfg {
   static constexpr int L_BYTES = kRows * kScK * 2;   // one logits tile, 16 KB
@@ -98,7 +103,7 @@ __global__ void sc_rowconst_kernel(const RowPartial* __restrict__ part, int rows
   rowc[r] = m * kLog2e + log2f(s);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kScThreads, 1)
 sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUtensorMap tm_e,
           const ScParams p) {
   using Cf = ScCfg;
@@ -126,7 +131,7 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScNL; ++s) {
       mbar_init(bar(Cf::B_L_FULL + s), 1);
-      mbar_init(bar(Cf::B_L_EMPTY + s), kRows);
+      mbar_init(bar(Cf::B_L_EMPTY + s), kScXform);
     }
     // an E slot is free once every CTA of the cluster has consumed it
     for (int s = 0; s < kScNE; ++s) {
@@ -134,11 +139,11 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
       mbar_init(bar(Cf::B_E_EMPTY + s), C);
     }
     for (int s = 0; s < kScNP; ++s) {
-      mbar_init(bar(Cf::B_P_FULL + s), kRows);
+      mbar_init(bar(Cf::B_P_FULL + s), kScXform);
       mbar_init(bar(Cf::B_P_EMPTY + s), 1);
     }
     mbar_init(bar(Cf::B_ACC_FULL), 1);
-    mbar_init(bar(Cf::B_ACC_EMPTY), kRows);
+    mbar_init(bar(Cf::B_ACC_EMPTY), kScXform);
     mbar_init(bar(Cf::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -247,11 +252,15 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
     umma_commit_warp(bar(Cf::B_DRAIN));
     drain_wait(bar(Cf::B_DRAIN), 0);
     __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------ probabilities and epilogue (one row each)
-    const int r = threadIdx.x;  // row of the tile == TMEM lane
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  } else {
+    // ---------------- probabilities and epilogue: warps 0-3 and 7-10; warp w
+    // owns TMEM lanes 32 (w % 4) .. +31 (one row each) and column half h
+    const int q = warp & 3;
+    const int h = warp < 4 ? 0 : 1;
+    const int r = q * 32 + lane;  // row of the tile == TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint64_t l2e2 = f32x2(kLog2e, kLog2e);
+    constexpr int kHalf = kScK / 2;  // logits per thread per block
     uint32_t l_stage = 0, l_phase = 0, g = 0, ui = 0;
     bool ok = true;
     for (int64_t u = cl; ok && u < U; u += ncl, ++ui) {
@@ -266,12 +275,12 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
           ok = false;
           break;
         }
-        // this row's 128 bytes; 16-byte chunk j sits at chunk j ^ (row & 7)
-        uint32_t x[kScK / 2];
+        // this row's half: 16-byte chunks 4h .. 4h+3, chunk j stored at j ^ (row & 7)
+        uint32_t x[kHalf / 2];
         const uint32_t rb = sL + l_stage * Cf::L_BYTES + r * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t a = rb + ((static_cast<uint32_t>(j) ^ (r & 7)) << 4);
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t a = rb + ((static_cast<uint32_t>(4 * h + j) ^ (r & 7)) << 4);
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(x[4 * j]), "=r"(x[4 * j + 1]), "=r"(x[4 * j + 2]), "=r"(x[4 * j + 3])
                        : "r"(a));
@@ -279,9 +288,9 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
         mbar_arrive(bar(Cf::B_L_EMPTY + l_stage));
         if (++l_stage == kScNL) { l_stage = 0; l_phase ^= 1; }
         // p = 2^(x log2(e) - c_r), two logits per fp32x2 FMA
-        uint32_t pk[kScK / 2];
+        uint32_t pk[kHalf / 2];
 #pragma unroll
-        for (int i = 0; i < kScK / 2; ++i) {
+        for (int i = 0; i < kHalf / 2; ++i) {
           float t0, t1;
           f32x2_split(fma_f32x2(f32x2(__uint_as_float(x[i] << 16), __uint_as_float(x[i] & 0xFFFF0000u)),
                                 l2e2, nc2),
@@ -291,8 +300,8 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
         if ((kb + 1) * kScK > p.vocab) {
           // the block past the vocabulary: those entries (zero-filled by TMA) get p = 0
 #pragma unroll
-          for (int i = 0; i < kScK / 2; ++i) {
-            const int v0 = kb * kScK + 2 * i;
+          for (int i = 0; i < kHalf / 2; ++i) {
+            const int v0 = kb * kScK + h * kHalf + 2 * i;
             if (v0 >= p.vocab) pk[i] = 0u;
             else if (v0 + 1 >= p.vocab) pk[i] &= 0xFFFFu;
           }
@@ -303,25 +312,27 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
           break;
         }
         tc_fence_after();
-        tmem_st32(lane_base + Cf::TM_P + ps * (kScK / 2), pk);
+        tmem_st16(lane_base + Cf::TM_P + ps * (kScK / 2) + h * (kHalf / 2), pk);
         tc_fence_before();
         mbar_arrive(bar(Cf::B_P_FULL + ps));
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
+      // this warp's 128 accumulator columns
       if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_ACC_FULL), ui & 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const int hc = h * (kScN / 2);
       if (p.splits == 1) {
         // one split: this row straight into out (small problems only)
-        const int col0 = w.nt * kScN;
+        const int col0 = w.nt * kScN + hc;
         float* dst = p.out + static_cast<size_t>(row) * p.d + col0;
 #pragma unroll 1
-        for (int cc = 0; cc < kScN / 32; ++cc) {
+        for (int cc = 0; cc < kScN / 64; ++cc) {
           uint32_t o[32];
-          tmem_ld32(lane_base + Cf::TM_ACC + cc * 32, o);
+          tmem_ld32(lane_base + Cf::TM_ACC + hc + cc * 32, o);
           if (row_ok) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -337,19 +348,14 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
         // column-major partial tile: for each column the warp writes 32
         // consecutive rows (128 bytes)
         float* dst = p.part + ((static_cast<size_t>(w.split) * p.m_tiles + w.mt) * p.n_tiles + w.nt) *
-                                  (static_cast<size_t>(kScN) * kRows) + r;
+                                  (static_cast<size_t>(kScN) * kRows) + static_cast<size_t>(hc) * kRows + r;
 #pragma unroll 1
-        for (int cc = 0; cc < kScN / 32; ++cc) {
+        for (int cc = 0; cc < kScN / 64; ++cc) {
           uint32_t o[32];
-          tmem_ld32(lane_base + Cf::TM_ACC + cc * 32, o);
+          tmem_ld32(lane_base + Cf::TM_ACC + hc + cc * 32, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) dst[static_cast<size_t>(cc * 32 + e) * kRows] = __uint_as_float(o[e]);
         }
-      } else {
-        // a cluster rank past the last row tile: nothing to write, but the
-        // accumulator is read like the others' before it is released
-        uint32_t o[32];
-        tmem_ld32(lane_base + Cf::TM_ACC, o);
       }
       tc_fence_before();
       mbar_arrive(bar(Cf::B_ACC_EMPTY));
