@@ -14,8 +14,8 @@
 //       moment read the same vocabulary range of logits and E and share it
 //       in L2.  Per 64-entry vocabulary block: TMA brings the 128 x 64 logits
 //       tile of this CTA's rows and 1/C of the 64 x 256 E tile (multicast to
-//       the cluster); eight warps, two per TMEM lane quadrant (one row and
-//       half of the block's columns per thread), turn the logits into bf16
+//       the cluster); several warps per TMEM lane quadrant (one row and a
+//       share of the block's columns per thread) turn the logits into bf16
 //       probabilities written straight to TMEM; the MMA warp accumulates
 //       P (A from TMEM) x E (B, N-major in shared memory) into TMEM.
 //   sc_combine_kernel: sums the splits' fp32 partials when there are several.
@@ -35,10 +35,11 @@ constexpr int kScK = 64;    // vocabulary entries per block (one 128-byte row of
 constexpr int kScNL = 3;    // logits ring stages (read into registers at once)
 constexpr int kScNE = 5;    // embedding ring stages (held until the MMA is done)
 constexpr int kScNP = 4;    // probability buffers in TMEM
-// warps 0-3 and 7-10 compute probabilities (two per TMEM lane quadrant, each
-// half of a block's columns); warps 4 / 6 load, warp 5 issues MMAs
-constexpr int kScThreads = 352;
-constexpr int kScXform = 256;  // probability threads
+// kScXW warps per TMEM lane quadrant compute probabilities, each 1/kScXW of a
+// block's columns: warps 0-3 and 7.. ; warps 4 / 6 load, warp 5 issues MMAs
+constexpr int kScXW = 2;
+constexpr int kScXform = 128 * kScXW;           // probability threads
+constexpr int kScThreads = kScXform + 3 * 32;
 
 struct ScCfg {
   static constexpr int L_BYTES = kRows * kScK * 2;   // one logits tile, 16 KB
@@ -69,6 +70,10 @@ struct ScParams {
   int rows, vocab, d;
   int m_tiles, n_tiles, m_groups, splits, kblocks;
 };
+
+// a thread's packed probabilities -> TMEM (8 or 16 columns, by share size)
+__device__ __forceinline__ void st_probs(uint32_t taddr, const uint32_t (&r)[8]) { tmem_st8(taddr, r); }
+__device__ __forceinline__ void st_probs(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
 
 struct ScUnit {
   int split, mt, nt, kb0, kb1;
@@ -253,14 +258,14 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
     drain_wait(bar(Cf::B_DRAIN), 0);
     __syncwarp();
   } else {
-    // ---------------- probabilities and epilogue: warps 0-3 and 7-10; warp w
-    // owns TMEM lanes 32 (w % 4) .. +31 (one row each) and column half h
+    // ---------------- probabilities and epilogue: warps 0-3 and 7.. ; warp w
+    // owns TMEM lanes 32 (w % 4) .. +31 (one row each) and column share h
     const int q = warp & 3;
-    const int h = warp < 4 ? 0 : 1;
+    const int h = (warp < 4 ? warp : warp - 3) >> 2;
     const int r = q * 32 + lane;  // row of the tile == TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint64_t l2e2 = f32x2(kLog2e, kLog2e);
-    constexpr int kHalf = kScK / 2;  // logits per thread per block
+    constexpr int kPart = kScK / kScXW;  // logits per thread per block
     uint32_t l_stage = 0, l_phase = 0, g = 0, ui = 0;
     bool ok = true;
     for (int64_t u = cl; ok && u < U; u += ncl, ++ui) {
@@ -275,12 +280,13 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
           ok = false;
           break;
         }
-        // this row's half: 16-byte chunks 4h .. 4h+3, chunk j stored at j ^ (row & 7)
-        uint32_t x[kHalf / 2];
+        // this row's share: 16-byte chunks (8/kScXW) h .. , chunk j stored at j ^ (row & 7)
+        constexpr int kChunks = kPart / 8;
+        uint32_t x[kPart / 2];
         const uint32_t rb = sL + l_stage * Cf::L_BYTES + r * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t a = rb + ((static_cast<uint32_t>(4 * h + j) ^ (r & 7)) << 4);
+        for (int j = 0; j < kChunks; ++j) {
+          const uint32_t a = rb + ((static_cast<uint32_t>(kChunks * h + j) ^ (r & 7)) << 4);
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(x[4 * j]), "=r"(x[4 * j + 1]), "=r"(x[4 * j + 2]), "=r"(x[4 * j + 3])
                        : "r"(a));
@@ -288,9 +294,9 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
         mbar_arrive(bar(Cf::B_L_EMPTY + l_stage));
         if (++l_stage == kScNL) { l_stage = 0; l_phase ^= 1; }
         // p = 2^(x log2(e) - c_r), two logits per fp32x2 FMA
-        uint32_t pk[kHalf / 2];
+        uint32_t pk[kPart / 2];
 #pragma unroll
-        for (int i = 0; i < kHalf / 2; ++i) {
+        for (int i = 0; i < kPart / 2; ++i) {
           float t0, t1;
           f32x2_split(fma_f32x2(f32x2(__uint_as_float(x[i] << 16), __uint_as_float(x[i] & 0xFFFF0000u)),
                                 l2e2, nc2),
@@ -300,8 +306,8 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
         if ((kb + 1) * kScK > p.vocab) {
           // the block past the vocabulary: those entries (zero-filled by TMA) get p = 0
 #pragma unroll
-          for (int i = 0; i < kHalf / 2; ++i) {
-            const int v0 = kb * kScK + h * kHalf + 2 * i;
+          for (int i = 0; i < kPart / 2; ++i) {
+            const int v0 = kb * kScK + h * kPart + 2 * i;
             if (v0 >= p.vocab) pk[i] = 0u;
             else if (v0 + 1 >= p.vocab) pk[i] &= 0xFFFFu;
           }
@@ -312,25 +318,25 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
           break;
         }
         tc_fence_after();
-        tmem_st16(lane_base + Cf::TM_P + ps * (kScK / 2) + h * (kHalf / 2), pk);
+        st_probs(lane_base + Cf::TM_P + ps * (kScK / 2) + h * (kPart / 2), pk);
         tc_fence_before();
         mbar_arrive(bar(Cf::B_P_FULL + ps));
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
-      // this warp's 128 accumulator columns
+      // this warp's share of the accumulator columns
       if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_ACC_FULL), ui & 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int hc = h * (kScN / 2);
+      const int hc = h * (kScN / kScXW);
       if (p.splits == 1) {
         // one split: this row straight into out (small problems only)
         const int col0 = w.nt * kScN + hc;
         float* dst = p.out + static_cast<size_t>(row) * p.d + col0;
 #pragma unroll 1
-        for (int cc = 0; cc < kScN / 64; ++cc) {
+        for (int cc = 0; cc < kScN / kScXW / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(lane_base + Cf::TM_ACC + hc + cc * 32, o);
           if (row_ok) {
@@ -350,7 +356,7 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
         float* dst = p.part + ((static_cast<size_t>(w.split) * p.m_tiles + w.mt) * p.n_tiles + w.nt) *
                                   (static_cast<size_t>(kScN) * kRows) + static_cast<size_t>(hc) * kRows + r;
 #pragma unroll 1
-        for (int cc = 0; cc < kScN / 64; ++cc) {
+        for (int cc = 0; cc < kScN / kScXW / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(lane_base + Cf::TM_ACC + hc + cc * 32, o);
 #pragma unroll
