@@ -585,8 +585,8 @@ dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   row_stats_kernel<<<static_cast<unsigned>(rows) * pl.chunks, kStatThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(logits), vocab, pl.chunks, stats);
-  sc_rowconst_kernel<<<(rows + 255) / 256, 256, 0, stream>>>(stats, rows, pl.chunks,
-                                                             const_cast<float*>(p.rowc));
+  sc_rowconst_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(stats, rows, pl.chunks,
+                                                         const_cast<float*>(p.rowc));
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
   if (e0 && cudaEventRecord(e0, stream) != cudaSuccess) return DG_ERR_CUDA;
@@ -605,7 +605,7 @@ dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const
   if (cudaLaunchKernelEx(&cfg, sc_kernel, ml, me, p) != cudaSuccess) return DG_ERR_CUDA;
   if (e1 && cudaEventRecord(e1, stream) != cudaSuccess) return DG_ERR_CUDA;
   if (pl.splits > 1) {
-    const dim3 grid((rows + 31) / 32, (d_model + 31) / 32);
+    const dim3 grid(pl.m_tiles, (d_model + 31) / 32);
     sc_combine_kernel<<<grid, dim3(32, 8), 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   }

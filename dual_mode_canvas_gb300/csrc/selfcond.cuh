@@ -93,19 +93,28 @@ __device__ __forceinline__ ScUnit sc_unit(const ScParams& p, int64_t u, int C, i
   return w;
 }
 
-// One thread per row: merge the row's chunk statistics in order and write
-// c_r = m log2(e) + log2(s).
-__global__ void sc_rowconst_kernel(const RowPartial* __restrict__ part, int rows, int chunks,
-                                   float* __restrict__ rowc) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= rows) return;
+// One warp per row: lane c merges chunks c, c + 32, ..., the lanes then
+// merge by shuffles and lane 0 writes c_r = m log2(e) + log2(s).
+__global__ void __launch_bounds__(256) sc_rowconst_kernel(const RowPartial* __restrict__ part, int rows,
+                                                           int chunks, float* __restrict__ rowc) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;  // warp-uniform
   float m = -INFINITY, s = 0.f, t = 0.f;
   int a = INT32_MAX;
-  for (int c = 0; c < chunks; ++c) {
+  for (int c = lane; c < chunks; c += 32) {
     const RowPartial q = part[static_cast<size_t>(r) * chunks + c];
     merge_stats(m, s, t, a, q.m, q.s, q.t, q.arg);
   }
-  rowc[r] = m * kLog2e + log2f(s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
+    const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
+    merge_stats(m, s, t, a, m2, s2, t2, a2);
+  }
+  if (lane == 0) rowc[r] = m * kLog2e + log2f(s);
 }
 
 __global__ void __launch_bounds__(kScThreads, 1)
@@ -378,34 +387,48 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
   if (C > 1) cluster_sync_all();
 }
 
-// out[r, c] = sum over splits of the partial tiles: a 32 x 32 block of out
-// per CTA, read along rows (the tiles are column-major), written along
-// columns through a shared-memory transpose.
-__global__ void __launch_bounds__(256) sc_combine_kernel(const ScParams p) {
-  __shared__ float t[32][33];
-  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+// out[r, c] = sum over splits of the partial tiles: one CTA per 128 rows x
+// 32 columns of out.  Each thread reads four rows of a column at a time
+// (the tiles are column-major, so a warp reads 512 contiguous bytes), sums
+// the splits, and the block writes out row by row through shared memory.
+__global__ void __launch_bounds__(256, 4) sc_combine_kernel(const ScParams p) {
+  __shared__ float t[32][kRows + 4];
+  const int mt = blockIdx.x, c0 = blockIdx.y * 32;
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
-  const int r = r0 + tx;
-  const int mt = r / kRows, rl = r - mt * kRows;
   const size_t tile = static_cast<size_t>(kScN) * kRows;
-  const size_t split_stride = static_cast<size_t>(p.m_tiles) * p.n_tiles * tile;
+  const size_t split_stride4 = static_cast<size_t>(p.m_tiles) * p.n_tiles * tile / 4;
+  const float4* src[4];
+  bool ok[4];
+  float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int c = c0 + ty + 8 * k;
-    float acc = 0.f;
-    if (r < p.rows && c < p.d) {
-      const int nt = c / kScN, cl = c - nt * kScN;
-      const float* src = p.part + (static_cast<size_t>(mt) * p.n_tiles + nt) * tile +
-                         static_cast<size_t>(cl) * kRows + rl;
-      for (int s = 0; s < p.splits; ++s) acc += src[s * split_stride];
-    }
-    t[ty + 8 * k][tx] = acc;
+    ok[k] = c < p.d;
+    const int nt = ok[k] ? c / kScN : 0, cl = ok[k] ? c - nt * kScN : 0;
+    src[k] = reinterpret_cast<const float4*>(p.part + (static_cast<size_t>(mt) * p.n_tiles + nt) * tile +
+                                             static_cast<size_t>(cl) * kRows) + tx;
+    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  __syncthreads();
+#pragma unroll 2
+  for (int s = 0; s < p.splits; ++s) {
+    float4 v[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int rr = r0 + ty + 8 * k, cc = c0 + tx;
-    if (rr < p.rows && cc < p.d) p.out[static_cast<size_t>(rr) * p.d + cc] = t[tx][ty + 8 * k];
+    for (int k = 0; k < 4; ++k) v[k] = ok[k] ? __ldg(src[k] + s * split_stride4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc[k].x += v[k].x;
+      acc[k].y += v[k].y;
+      acc[k].z += v[k].z;
+      acc[k].w += v[k].w;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) *reinterpret_cast<float4*>(&t[ty + 8 * k][4 * tx]) = acc[k];
+  __syncthreads();
+  const int c = c0 + tx;
+  for (int rr = ty; rr < kRows; rr += 8) {
+    const int row = mt * kRows + rr;
+    if (row < p.rows && c < p.d) p.out[static_cast<size_t>(row) * p.d + c] = t[tx][rr];
   }
 }
 
