@@ -70,8 +70,9 @@ def algorithmic_flops(wl) -> int:
     return 4 * wl.head_dim * wl.num_q_heads * visible_pairs(wl)
 
 
-def algorithmic_bytes(wl) -> int:
-    """Q + out (bf16) + lse (fp32) + every K/V row some query sees, read once per KV head."""
+def algorithmic_bytes(wl, qkv_bytes: int = 2) -> int:
+    """Q + out (bf16) + lse (fp32) + every K/V row some query sees, read once per KV head
+    (Q, K, V of ``qkv_bytes`` per element: 2 for bf16, 1 for e4m3)."""
     W = wl.window
     kv = 0
     for c, n, md in wl.seqs:
@@ -79,8 +80,9 @@ def algorithmic_bytes(wl) -> int:
         lo = 0 if W < 0 else max(0, c - W)
         hi = c + n - 1 if md == wls.CAUSAL else (L - 1 if W < 0 else min(L - 1, c + n - 1 + W))
         kv += hi - lo + 1
-    q = wl.total_q * wl.num_q_heads * wl.head_dim * 2
-    return 2 * q + wl.total_q * wl.num_q_heads * 4 + 2 * kv * wl.num_kv_heads * wl.head_dim * 2
+    q = wl.total_q * wl.num_q_heads * wl.head_dim
+    return (q * qkv_bytes + q * 2 + wl.total_q * wl.num_q_heads * 4 +
+            2 * kv * wl.num_kv_heads * wl.head_dim * qkv_bytes)
 
 
 def load_peaks():
@@ -217,7 +219,16 @@ def run_gpu(args):
     binding.load_library()
     dev = torch.device("cuda")
     paged = args.paged > 0
-    if paged:
+    fp8 = args.fp8
+    if fp8 and paged:
+        raise SystemExit("--fp8 runs on the contiguous layout only")
+    if fp8:
+        # e4m3 codes with one scale per tensor; later canvases use step 0's scales
+        batch = wls.make_fp8_batch(wl, device="cuda")
+        q, k, v = batch["q8"], batch["k8"], batch["v8"]
+        sc8 = (batch["q_scale"], batch["k_scale"], batch["v_scale"])
+        rows = wls.canvas_rows(wl)
+    elif paged:
         # paged KV cache: the step's canvas K/V go in as k_new / v_new and the
         # call appends them into their pages (inside the timed call)
         batch = wls.make_paged_batch(wl, args.paged, device="cuda")
@@ -243,8 +254,12 @@ def run_gpu(args):
                 vc = torch.cat([v[a:b] for a, b in rows])
             else:
                 qs, kc, vc = wls.denoise_step_inputs(wl, step, device="cuda")
+                if fp8:
+                    qs = wls.quantize_e4m3(qs.float(), sc8[0])
+                    kc = wls.quantize_e4m3(kc.float(), sc8[1])
+                    vc = wls.quantize_e4m3(vc.float(), sc8[2])
             canv.append((qs, kc, vc))
-    out = torch.empty_like(q)
+    out = torch.empty((wl.total_q, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((wl.total_q, wl.num_q_heads), dtype=torch.float32, device=dev)
     ws = torch.empty(binding.workspace_size(len(wl.seqs), wl.total_q, wl.num_q_heads,
                                             wl.num_kv_heads, wl.head_dim), dtype=torch.uint8,
@@ -264,7 +279,10 @@ def run_gpu(args):
         flush.fill_(s & 0xFF)
 
     def call(events=None):
-        if paged:
+        if fp8:
+            binding.forward_fp8(q, k, v, cu_q, ctx, mode, wl.window, wl.scale, *sc8, out=out, lse=lse,
+                                workspace=ws, events=events)
+        elif paged:
             binding.forward_paged(q, k, v, k_cache, v_cache, bt, cu_q, ctx, mode, wl.window, wl.scale,
                                   out=out, lse=lse, workspace=ws, events=events)
         else:
@@ -272,7 +290,7 @@ def run_gpu(args):
                             workspace=ws, events=events)
 
     flops = algorithmic_flops(wl)
-    nbytes = algorithmic_bytes(wl)
+    nbytes = algorithmic_bytes(wl, 1 if fp8 else 2)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(nsteps)]
@@ -315,6 +333,7 @@ def run_gpu(args):
         hq = [c[0].cpu().pin_memory() for c in canv]
         hk = [c[1].cpu().pin_memory() for c in canv]
         hv = [c[2].cpu().pin_memory() for c in canv]
+        esz = hq[0].element_size()
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         kc_dev = torch.empty_like(canv[0][1])
@@ -340,7 +359,7 @@ def run_gpu(args):
             if s >= args.warmup:
                 e2e_ms.append(e0.elapsed_time(e1))
         e2e_tot = max_over_ranks(world, float(sum(e2e_ms)))
-        h2d = hq[0].numel() * 2 + hk[0].numel() * 2 + hv[0].numel() * 2
+        h2d = (hq[0].numel() + hk[0].numel() + hv[0].numel()) * esz
         d2h = h_out.numel() * 2 + h_lse.numel() * 4
         e2e = {"value": world * flops * args.steps / (e2e_tot * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -353,6 +372,8 @@ def run_gpu(args):
     attn_tflops = flops / (attn_avg_ms * 1e-3) / 1e12
     sustained = args.steps * ms_per_step > 1000.0
     tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    if fp8:
+        tc_peak = tc_peak * 2.0  # the nominal e4m3 / bf16 dense ratio (4.5 / 2.25 PFLOP/s)
     t_tc = flops / (tc_peak * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if t_tc >= t_hbm else "hbm"
@@ -364,7 +385,8 @@ def run_gpu(args):
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(gbs / peaks["hbm_gbs"], 4)}
     roof["traffic"] = None if paged else NCU_TRAFFIC_BYTES.get(args.workload)
-    roof["peak_source"] = f"{peaks_src} ({'sustained' if (sustained and bound == 'tensor') else 'burst'})"
+    roof["peak_source"] = f"{peaks_src} ({'sustained' if (sustained and bound == 'tensor') else 'burst'})" + (
+        "; e4m3 peak = measured bf16 x 2 (nominal ratio)" if fp8 else "")
     roof["kernel"] = "fwd_kernel (persistent tcgen05 attention)"
     roof["kernel_ms_per_launch"] = round(attn_avg_ms, 4)
     roof["tighter_roof_frac"] = round(max(t_tc, t_hbm) / (attn_avg_ms * 1e-3), 4)
@@ -372,8 +394,9 @@ def run_gpu(args):
     res = {
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1), bf16)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1), e4m3 with one scale per tensor)" if fp8 else
+                "synthetic (seeded N(0,1), bf16)",
         "config": {"workload": wl.name, "seqs_ctx_nq_mode": [list(s) for s in wl.seqs],
                    "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
                    "head_dim": wl.head_dim, "window": wl.window,
@@ -683,6 +706,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--fp8", action="store_true",
+                    help="run the attention in e4m3 (Q, K, V codes with one scale per tensor)")
     ap.add_argument("--paged", type=int, default=0,
                     help="page size: run the step through the paged KV cache (0: contiguous)")
     ap.add_argument("--workload", default="denoise_loop",

@@ -28,6 +28,7 @@ DG_MODE_BIDIRECTIONAL = 1
 
 EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profiled",
             "dg_attn_forward_noalloc", "dg_attn_forward_paged", "dg_attn_forward_paged_profiled",
+            "dg_attn_forward_fp8", "dg_attn_forward_fp8_profiled",
             "dg_selfcond_workspace_size", "dg_selfcond_forward", "dg_selfcond_forward_profiled",
             "dg_accept_workspace_size", "dg_accept_step",
             "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
@@ -65,6 +66,12 @@ def load_library():
     lib.dg_attn_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                             i32, ctypes.c_float, vp, vp, vp]
     lib.dg_attn_forward_noalloc.restype = ctypes.c_int
+    lib.dg_attn_forward_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                        ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                        ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.dg_attn_forward_fp8.restype = ctypes.c_int
+    lib.dg_attn_forward_fp8_profiled.argtypes = lib.dg_attn_forward_fp8.argtypes + [vp, vp]
+    lib.dg_attn_forward_fp8_profiled.restype = ctypes.c_int
     lib.dg_attn_forward_paged.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, i32, vp, vp, vp, i32,
                                           i32, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, sz,
                                           vp]
@@ -162,6 +169,46 @@ def forward(q, k, v, cu_q, ctx_len, mode, window: int, scale: float, *, out=None
         rc = lib.dg_attn_forward_profiled(*args, events[0].cuda_event, events[1].cuda_event)
     if rc != DG_OK:
         raise DgAttnError(rc, "dg_attn_forward")
+    return out, lse
+
+
+def forward_fp8(q8, k8, v8, cu_q, ctx_len, mode, window: int, scale: float, q_scale: float,
+                k_scale: float, v_scale: float, *, out=None, lse=None, workspace=None, stream=None,
+                events=None):
+    """FP8 variant through ``dg_attn_forward_fp8``: q8 / k8 / v8 are e4m3 codes
+    (uint8 or torch.float8_e4m3fn) shaped like the bf16 inputs, with one fp32
+    scale per tensor.  Returns ``(out bf16, lse fp32)``."""
+    lib = load_library()
+    q8, k8, v8 = (t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t for t in (q8, k8, v8))
+    for name, t, dt in (("q8", q8, torch.uint8), ("k8", k8, torch.uint8), ("v8", v8, torch.uint8),
+                        ("cu_q", cu_q, torch.int32), ("ctx_len", ctx_len, torch.int32),
+                        ("mode", mode, torch.uint8)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    total_q, Hq, D = q8.shape
+    total_kv, Hkv, Dk = k8.shape
+    if tuple(v8.shape) != (total_kv, Hkv, Dk) or Dk != D:
+        raise ValueError("k8 and v8 must both be [total_kv, Hkv, D]")
+    B = ctx_len.numel()
+    if out is None:
+        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q8.device)
+    need = lib.dg_attn_workspace_size(B, total_q, Hq, Hkv, D)
+    if need == 0:
+        raise DgAttnError(DG_ERR_INVALID_ARG, "dg_attn_workspace_size")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q8.device)
+    args = (_ptr(q8), _ptr(k8), _ptr(v8), _ptr(cu_q), _ptr(ctx_len), _ptr(mode), B, total_q, total_kv,
+            Hq, Hkv, D, int(window), float(scale), float(q_scale), float(k_scale), float(v_scale),
+            _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream))
+    if events is None:
+        rc = lib.dg_attn_forward_fp8(*args)
+    else:
+        rc = lib.dg_attn_forward_fp8_profiled(*args, events[0].cuda_event, events[1].cuda_event)
+    if rc != DG_OK:
+        raise DgAttnError(rc, "dg_attn_forward_fp8")
     return out, lse
 
 

@@ -38,7 +38,7 @@ int dim_slot(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
-  int max_clusters[3][4] = {};  // [head_dim][cluster size]: co-resident clusters
+  int max_clusters[2][3][4] = {};  // [e4m3][head_dim][cluster size]: co-resident clusters
   int sc_max_clusters[2] = {};  // self-conditioning kernel, clusters of 1 / 2
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;   // device address of g_status
@@ -52,20 +52,24 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // Per-head_dim kernel shapes: KV tile rows (TMEM holds O, two S/P buffers of
 // BN columns and Q) and K-ring / V-ring stages (shared memory holds only the
 // rings, up to 224 KB).
-template <int D> struct Shape;
+// e4m3 tiles are half the bytes: the same rings hold more stages.
+template <int D, bool F8 = false> struct Shape;
 template <> struct Shape<64> { static constexpr int BN = 128, NK = 6, NV = 6; };
 template <> struct Shape<128> { static constexpr int BN = 128, NK = 4, NV = 3; };
 template <> struct Shape<256> { static constexpr int BN = 64, NK = 4, NV = 3; };
+template <> struct Shape<128, true> { static constexpr int BN = 128, NK = 6, NV = 6; };
+template <> struct Shape<256, true> { static constexpr int BN = 64, NK = 6, NV = 6; };
 
-int kv_tile_rows(int D) {
+int kv_tile_rows(int D, bool f8 = false) {
+  if (f8) return D == 128 ? Shape<128, true>::BN : Shape<256, true>::BN;
   return D == 64 ? Shape<64>::BN : D == 128 ? Shape<128>::BN : Shape<256>::BN;
 }
 
-template <int D>
+template <int D, bool F8 = false>
 cudaError_t set_kernel_attrs(DeviceInfo& di) {
-  using S = Shape<D>;
-  using C = FwdCfg<D, S::BN, S::NK, S::NV>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV>,
+  using S = Shape<D, F8>;
+  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8>;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   // how many clusters of each size fit on the device at once (persistent grid)
@@ -82,9 +86,9 @@ cudaError_t set_kernel_attrs(DeviceInfo& di) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel<D, S::BN, S::NK, S::NV>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel<D, S::BN, S::NK, S::NV, F8>, &cfg) != cudaSuccess)
       n = 0;
-    di.max_clusters[dim_slot(D)][cluster_slot(cs)] = n;
+    di.max_clusters[F8 ? 1 : 0][dim_slot(D)][cluster_slot(cs)] = n;
   }
   cudaGetLastError();
   return cudaSuccess;
@@ -140,7 +144,8 @@ dg_status_t device_info(DeviceInfo** out) {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     if (set_kernel_attrs<64>(di) != cudaSuccess || set_kernel_attrs<128>(di) != cudaSuccess ||
-        set_kernel_attrs<256>(di) != cudaSuccess || set_sc_attrs(di) != cudaSuccess)
+        set_kernel_attrs<256>(di) != cudaSuccess || set_kernel_attrs<128, true>(di) != cudaSuccess ||
+        set_kernel_attrs<256, true>(di) != cudaSuccess || set_sc_attrs(di) != cudaSuccess)
       return DG_ERR_CUDA;
     void* sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status) != cudaSuccess) return DG_ERR_CUDA;
@@ -158,20 +163,20 @@ dg_status_t device_info(DeviceInfo** out) {
 
 // Cluster size for a call: C query tiles of one (sequence, KV head) share
 // every K/V load.  DG_ATTN_CLUSTER (1, 2, 4 or 8) overrides the default.
-int cluster_for(const DeviceInfo& di, int D) {
+int cluster_for(const DeviceInfo& di, int D, bool f8 = false) {
   int C = 2;
   if (const char* e = std::getenv("DG_ATTN_CLUSTER")) {
     const int v = std::atoi(e);
     if (v == 1 || v == 2 || v == 4 || v == 8) C = v;
   }
-  while (C > 1 && di.max_clusters[dim_slot(D)][cluster_slot(C)] < 1) C >>= 1;
+  while (C > 1 && di.max_clusters[f8 ? 1 : 0][dim_slot(D)][cluster_slot(C)] < 1) C >>= 1;
   return C;
 }
 
 // Persistent grid: as many clusters as are co-resident (DG_ATTN_NUM_CTAS caps
 // the number of CTAs, for tests of the split-KV path).
-int num_clusters_for(const DeviceInfo& di, int D, int C) {
-  int n = C == 1 ? di.num_sms : di.max_clusters[dim_slot(D)][cluster_slot(C)];
+int num_clusters_for(const DeviceInfo& di, int D, int C, bool f8 = false) {
+  int n = C == 1 ? di.num_sms : di.max_clusters[f8 ? 1 : 0][dim_slot(D)][cluster_slot(C)];
   if (n < 1) n = 1;
   if (const char* e = std::getenv("DG_ATTN_NUM_CTAS")) {
     const int v = std::max(1, std::atoi(e) / C);
@@ -212,29 +217,32 @@ bool sizes_ok(int B, int total_q, int Hq, int Hkv, int D) {
   return true;
 }
 
-// [rows, heads, D] bf16 tensor map, box {64, box_heads, box_rows}, 128-byte swizzle.
+// [rows, heads, D] tensor map of bf16 (or, with e4m3, of bytes), box {one
+// 128-byte block of D, box_heads, box_rows}, 128-byte swizzle.
 dg_status_t encode_map(CUtensorMap* map, const void* base, int rows, int heads, int D,
-                       int box_heads, int box_rows) {
+                       int box_heads, int box_rows, bool e4m3 = false) {
+  const cuuint64_t es = e4m3 ? 1 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                                 static_cast<cuuint64_t>(heads) * D * 2};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_heads),
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * es,
+                                 static_cast<cuuint64_t>(heads) * D * es};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box_heads),
                              static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  const CUresult r = g_encode(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              3, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DG_OK : DG_ERR_INVALID_ARG;
 }
 
-template <int D>
+template <int D, bool F8 = false>
 dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
                    const FwdParams& p, int num_clusters, int max_groups, cudaStream_t stream,
                    cudaEvent_t ev_begin, cudaEvent_t ev_end) {
-  using S = Shape<D>;
-  using C = FwdCfg<D, S::BN, S::NK, S::NV>;
+  using S = Shape<D, F8>;
+  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8>;
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DG_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_clusters * p.C);
@@ -248,7 +256,7 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV>, mk, mv, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV, F8>, mk, mv, p) != cudaSuccess)
     return DG_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return DG_ERR_CUDA;
   const dim3 cgrid(max_groups * p.C, (kRows + kCombineWarps - 1) / kCombineWarps);
@@ -282,7 +290,10 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
                          int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale,
                          void* out, float* lse, void* workspace, size_t workspace_bytes,
                          void* stream_ptr, void* ev_begin, void* ev_end,
-                         const PagedArgs* pg = nullptr) {
+                         const PagedArgs* pg = nullptr, const float* e4m3_scales = nullptr) {
+  // e4m3_scales = {q, k, v} scales: Q, K, V are e4m3 bytes (contiguous layout only)
+  const bool f8 = e4m3_scales != nullptr;
+  if (f8 && (head_dim == 64 || pg)) return DG_ERR_UNSUPPORTED;
   if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim))
     return (num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
             num_q_heads / num_kv_heads > kRows) || (head_dim > 0 && head_dim != 64 &&
@@ -307,8 +318,8 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
 
   const int G = num_q_heads / num_kv_heads;
   const int TT = kRows / G;
-  const int BN = kv_tile_rows(head_dim);
-  const int Ccl = cluster_for(*di, head_dim);
+  const int BN = kv_tile_rows(head_dim, f8);
+  const int Ccl = cluster_for(*di, head_dim, f8);
   CUtensorMap mk, mv;
   // each CTA of a cluster loads BN / C rows of every K/V tile; from a paged
   // cache in boxes of at most one page
@@ -317,8 +328,8 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   const void* kmap = pg ? pg->k_cache : k;
   const void* vmap = pg ? pg->v_cache : v;
   const int map_rows = pg ? (pg->num_pages << pg->page_shift) : total_kv;
-  if (encode_map(&mk, kmap, map_rows, num_kv_heads, head_dim, 1, box) != DG_OK ||
-      encode_map(&mv, vmap, map_rows, num_kv_heads, head_dim, 1, box) != DG_OK)
+  if (encode_map(&mk, kmap, map_rows, num_kv_heads, head_dim, 1, box, f8) != DG_OK ||
+      encode_map(&mv, vmap, map_rows, num_kv_heads, head_dim, 1, box, f8) != DG_OK)
     return DG_ERR_INVALID_ARG;
 
   uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -330,7 +341,7 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.ws.unit_begin = reinterpret_cast<int64_t*>(w + lay.unit_begin);
   p.ws.part_lse = reinterpret_cast<float*>(w + lay.part_lse);
   p.ws.part_o = reinterpret_cast<float*>(w + lay.part_o);
-  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.q = q;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.status = di->status;
@@ -344,8 +355,11 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.page_box = box;
   p.debug_skip_k_load = -1;
   if (const char* e = std::getenv("DG_ATTN_DEBUG_SKIP_K_LOAD")) p.debug_skip_k_load = std::atoi(e);
-  p.scale = scale;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  // e4m3: the q and k scales multiply every score, the v scale the output
+  const float s_eff = f8 ? scale * e4m3_scales[0] * e4m3_scales[1] : scale;
+  p.scale = s_eff;
+  p.scale_log2 = s_eff * 1.4426950408889634f;
+  p.v_scale = f8 ? e4m3_scales[2] : 1.f;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   PagedArgs pa = {};
@@ -361,8 +375,12 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
       cu_q, ctx_len, mode, num_seqs, total_q, pg ? INT32_MAX : total_kv, num_kv_heads, TT, BN,
       window, lay.max_tiles, Ccl, p.ws, pa, p.status);
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
-  const int num_clusters = num_clusters_for(*di, head_dim, Ccl);
+  const int num_clusters = num_clusters_for(*di, head_dim, Ccl, f8);
   cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
+  if (f8) {
+    if (head_dim == 128) return launch<128, true>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
+    return launch<256, true>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
+  }
   switch (head_dim) {
     case 64: return launch<64>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
     case 128: return launch<128>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
@@ -416,6 +434,47 @@ extern "C" dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, con
   return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
                       num_kv_heads, head_dim, window, scale, out, lse, di->noalloc_scratch,
                       DG_ATTN_NOALLOC_SCRATCH_BYTES, stream, nullptr, nullptr);
+}
+
+namespace {
+dg_status_t forward_fp8(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                        const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
+                        int32_t total_q, int32_t total_kv, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t window, float scale, float q_scale, float k_scale,
+                        float v_scale, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream, void* ev_begin, void* ev_end) {
+  if (!(q_scale > 0.f) || !(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(q_scale) ||
+      !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return DG_ERR_INVALID_ARG;
+  const float sc[3] = {q_scale, k_scale, v_scale};
+  return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
+                      num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
+                      stream, ev_begin, ev_end, nullptr, sc);
+}
+}  // namespace
+
+extern "C" dg_status_t dg_attn_forward_fp8(const void* q, const void* k, const void* v,
+                                           const int32_t* cu_q, const int32_t* ctx_len,
+                                           const uint8_t* mode, int32_t num_seqs, int32_t total_q,
+                                           int32_t total_kv, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_dim, int32_t window,
+                                           float scale, float q_scale, float k_scale, float v_scale,
+                                           void* out, float* lse, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  return forward_fp8(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
+                     num_kv_heads, head_dim, window, scale, q_scale, k_scale, v_scale, out, lse,
+                     workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+extern "C" dg_status_t dg_attn_forward_fp8_profiled(
+    const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* ctx_len,
+    const uint8_t* mode, int32_t num_seqs, int32_t total_q, int32_t total_kv, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale, float q_scale,
+    float k_scale, float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+    void* stream, void* attn_begin_event, void* attn_end_event) {
+  return forward_fp8(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
+                     num_kv_heads, head_dim, window, scale, q_scale, k_scale, v_scale, out, lse,
+                     workspace, workspace_bytes, stream, attn_begin_event, attn_end_event);
 }
 
 namespace {

@@ -90,7 +90,7 @@ struct Workspace {
 
 struct FwdParams {
   Workspace ws;
-  const __nv_bfloat16* q;
+  const void* q;       // bf16 or e4m3 [total_q, Hq, D]
   __nv_bfloat16* out;
   float* lse;
   int* status;
@@ -102,8 +102,14 @@ struct FwdParams {
   // >= 0: the K loader skips the TMA load of this (per-CTA) KV tile, so the
   // MMA warp's bounded wait for it expires (tests of the timeout path)
   int debug_skip_k_load;
-  float scale, scale_log2;
+  float scale, scale_log2;  // softmax scale (times the q and k scales for e4m3 inputs)
+  float v_scale;            // e4m3 inputs: the v scale, applied in the epilogue (1 for bf16)
 };
+
+// a row of packed P -> TMEM (16, 32 or 64 columns)
+__device__ __forceinline__ void store_packed_p(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
+__device__ __forceinline__ void store_packed_p(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
+__device__ __forceinline__ void store_packed_p(uint32_t taddr, const uint32_t (&r)[64]) { tmem_st64(taddr, r); }
 
 __device__ __forceinline__ void record_error(int* status, int code) {
   atomicCAS(status, 0, code);
@@ -404,11 +410,29 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // -------------------------------------------------------------- main kernel
+// Element type of Q, K, V and of P: bf16 (tcgen05 kind::f16) or e4m3
+// (kind::f8f6f4).  Sizes in elements of the 128-byte swizzle block, of one
+// MMA K step (32 bytes) and of one 32-bit TMEM column.
+template <bool F8>
+struct Elem {
+  static constexpr int SIZE = F8 ? 1 : 2;
+  static constexpr int BLK = 128 / SIZE;
+  static constexpr int KSTEP = 32 / SIZE;
+  static constexpr int PER_WORD = 4 / SIZE;
+  // e4m3 P: probabilities are scaled by 2^P_SHIFT so the small ones stay in
+  // the normal range, and the running maximum is refreshed once it grew by
+  // more than 2^LAZY, so a scaled P never exceeds 2^(LAZY + P_SHIFT) = 256
+  // (the largest e4m3 is 448)
+  static constexpr int P_SHIFT = F8 ? 5 : 0;
+  static constexpr float LAZY = F8 ? 3.f : 8.f;
+};
+
 // Shared memory holds only the K and V rings; Q, S, P and O live in TMEM.
-template <int D, int BN, int NK, int NV>
+template <int D, int BN, int NK, int NV, bool F8 = false>
 struct FwdCfg {
-  static constexpr int NKB = D / 64;                 // 128-byte column blocks of head_dim
-  static constexpr int KV_BYTES = BN * D * 2;        // one K (or V) tile
+  using E = Elem<F8>;
+  static constexpr int NKB = D * E::SIZE / 128;      // 128-byte column blocks of head_dim
+  static constexpr int KV_BYTES = BN * D * E::SIZE;  // one K (or V) tile
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
@@ -422,19 +446,21 @@ struct FwdCfg {
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
   // TMEM columns: O (fp32, D), two S buffers (fp32, BN; P overwrites the first
-  // BN/2 columns as packed bf16 pairs), Q (packed bf16 pairs, D/2)
+  // BN / PER_WORD columns, packed), Q (packed, D / PER_WORD)
   static constexpr uint32_t TM_O = 0, TM_S0 = D, TM_S1 = D + BN, TM_Q = D + 2 * BN;
   static_assert(D % 64 == 0 && D >= 64 && D <= 256, "head_dim");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "kv tile");
-  static_assert(D + 2 * BN + D / 2 <= static_cast<int>(kTmemCols), "TMEM budget");
+  static_assert(NKB >= 1, "head_dim of at least one 128-byte block");
+  static_assert(D + 2 * BN + D / E::PER_WORD <= static_cast<int>(kTmemCols), "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <int D, int BN, int NK, int NV>
+template <int D, int BN, int NK, int NV, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const FwdParams p) {
-  using Cf = FwdCfg<D, BN, NK, NV>;
+  using Cf = FwdCfg<D, BN, NK, NV, F8>;
+  using E = Elem<F8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -536,8 +562,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             const TileDesc tn = p.ws.tiles[static_cast<size_t>(nx.tile) * C + rank];
             const int ntok = max(tn.n_tok, 1);
             for (int t = 0; t < ntok; ++t)
-              prefetch_l2_bulk(p.q + (static_cast<size_t>(tn.q_row0 + t) * p.Hq + tn.kvh * G) * D,
-                               static_cast<uint32_t>(G * D * 2));
+              prefetch_l2_bulk(static_cast<const uint8_t*>(p.q) +
+                                   (static_cast<size_t>(tn.q_row0 + t) * p.Hq + tn.kvh * G) * D * E::SIZE,
+                               static_cast<uint32_t>(G * D * E::SIZE));
           }
         }
         for (int j = sg.j0; j < sg.j1; ++j) {
@@ -553,10 +580,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 #pragma unroll
             for (int kb = 0; kb < Cf::NKB; ++kb) {
               if (C > 1)
-                tma_load_3d_multicast(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh,
+                tma_load_3d_multicast(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * E::BLK, td.kvh,
                                       row, cta_mask);
               else
-                tma_load_3d(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh, row);
+                tma_load_3d(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * E::BLK, td.kvh, row);
             }
           } else {
             // positions past the sequence's last key read its last page
@@ -572,10 +599,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 #pragma unroll
               for (int kb = 0; kb < Cf::NKB; ++kb) {
                 if (C > 1)
-                  tma_load_3d_multicast(d0 + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh,
+                  tma_load_3d_multicast(d0 + kb * (BN * 128), map, full0 + 8u * stage, kb * E::BLK, td.kvh,
                                         row, cta_mask);
                 else
-                  tma_load_3d(d0 + kb * (BN * 128), map, full0 + 8u * stage, kb * 64, td.kvh, row);
+                  tma_load_3d(d0 + kb * (BN * 128), map, full0 + 8u * stage, kb * E::BLK, td.kvh, row);
               }
             }
           }
@@ -600,8 +627,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // (warp-uniform) operands and one elected lane issues each tcgen05 op:
     // issuing from a single divergent lane cost ~100 clocks per MMA.
     {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, BN, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, D, 0, 1);
+      constexpr uint32_t idesc_qk = F8 ? idesc_e4m3_f32(kRows, BN, 0, 0) : idesc_bf16_f32(kRows, BN, 0, 0);
+      constexpr uint32_t idesc_pv = F8 ? idesc_e4m3_f32(kRows, D, 0, 1) : idesc_bf16_f32(kRows, D, 0, 1);
       uint32_t k_stage = 0, k_phase = 0, v_stage = 0, v_phase = 0;
       uint32_t gj = 0;
       int seg_i = 0;
@@ -619,9 +646,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             const uint32_t d_s = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
             const uint32_t k_base = sK + k_stage * Cf::KV_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < D / E::KSTEP; ++kk) {
               const uint64_t b = smem_desc_sw128(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-              umma_bf16_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
+              if constexpr (F8) umma_e4m3_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
+              else umma_bf16_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
             }
             umma_commit_warp(bar(Cf::B_S_FULL + (g & 1)));
             if (C > 1) umma_commit_multicast_warp(bar(Cf::B_K_EMPTY + k_stage), cta_mask);
@@ -639,9 +667,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             const uint32_t p_tm = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
             const uint32_t v_base = sV + v_stage * Cf::KV_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t b = smem_desc_sw128(v_base + kk * 2048, BN * 128, 1024);
-              umma_bf16_ts_warp(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+            for (int kk = 0; kk < BN / E::KSTEP; ++kk) {
+              const uint64_t b = smem_desc_sw128(v_base + kk * (E::KSTEP * 128), BN * 128, 1024);
+              if constexpr (F8)
+                umma_e4m3_ts_warp(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+              else
+                umma_bf16_ts_warp(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
             }
             umma_commit_warp(bar(Cf::B_O_DONE + (g & 1)));
             if (C > 1) umma_commit_multicast_warp(bar(Cf::B_V_EMPTY + v_stage), cta_mask);
@@ -672,14 +703,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // This thread's row of a tile's Q, staged in registers as packed bf16
     // pairs: the loads of the next segment's row are issued at the start of
     // this segment's epilogue and land while O is drained.
-    uint32_t qw[D / 2];
+    constexpr int kQW = D / E::PER_WORD;  // packed 32-bit words of a Q row
+    uint32_t qw[kQW];
     auto q_issue = [&](const TileDesc& t) {
       const int ntq = max(t.n_tok, 1);
       const int hq = t.kvh * G + (r < G * TT ? g_row : 0);
       const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<size_t>(t.q_row0 + min(t_row, ntq - 1)) * p.Hq + hq) * D);
+          static_cast<const uint8_t*>(p.q) +
+          (static_cast<size_t>(t.q_row0 + min(t_row, ntq - 1)) * p.Hq + hq) * D * E::SIZE);
 #pragma unroll
-      for (int e = 0; e < D / 8; ++e) {
+      for (int e = 0; e < kQW / 4; ++e) {
         const uint4 x = __ldg(src + e);
         qw[4 * e + 0] = x.x; qw[4 * e + 1] = x.y; qw[4 * e + 2] = x.z; qw[4 * e + 3] = x.w;
       }
@@ -687,7 +720,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // registers -> TMEM Q columns; the MMA warp may start QK^T after this
     auto q_commit = [&]() {
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
+      for (int c = 0; c < kQW / 32; ++c)
         tmem_st32(lane_base + Cf::TM_Q + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&qw[c * 32]));
       tc_fence_before();
       mbar_arrive(bar(Cf::B_Q_FULL));
@@ -750,12 +783,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         bool rescale = false;
         if (m_run == -INFINITY) {
           m_use = m_new;
-        } else if ((m_new - m_run) * sl2 > 8.f) {
+        } else if ((m_new - m_run) * sl2 > E::LAZY) {
           m_use = m_new;
           alpha = ex2_approx((m_run - m_new) * sl2);
           rescale = true;
         }
-        const float base = (m_use == -INFINITY) ? 0.f : m_use * sl2;
+        const float base = (m_use == -INFINITY) ? 0.f : m_use * sl2 - static_cast<float>(E::P_SHIFT);
         // p = 2^(s * scale * log2(e) - base), two lanes per fp32x2 instruction;
         // the row sum runs in four independent fp32x2 accumulators.  With 128
         // keys per tile the MUFU ex2 rate alone would match the MMA time, so 3
@@ -763,7 +796,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         constexpr int kPolyPairs = BN == 128 ? 3 : 0;
         const uint64_t sl2x2 = f32x2(sl2, sl2), nbase2 = f32x2(-base, -base);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[BN / 2];
+        uint32_t pk[BN / E::PER_WORD];
 #pragma unroll
         for (int c = 0; c < BN; c += 2) {
           float t0, t1, p0, p1;
@@ -774,7 +807,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             p0 = ex2_approx(t0);
             p1 = ex2_approx(t1);
           }
-          pk[c / 2] = pack_bf16x2(p0, p1);
+          if constexpr (F8) {
+            // e4m3 pairs, two per 32-bit word, lower key in the lower byte
+            const uint32_t h = pack_e4m3x2(p0, p1);
+            if (((c >> 1) & 1) == 0) pk[c / 4] = h;
+            else pk[c / 4] |= h << 16;
+          } else {
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
           acc[(c >> 1) & 3] = add_f32x2(acc[(c >> 1) & 3], f32x2(p0, p1));
         }
         float a0, a1, a2, a3, a4, a5, a6, a7;
@@ -800,8 +840,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           }
         }
         // P row (bf16 pairs) over the first BN/2 columns of this S buffer
-        if constexpr (BN == 64) tmem_st32(s_addr, pk);
-        else tmem_st64(s_addr, pk);
+        store_packed_p(s_addr, pk);
         tc_fence_before();
         mbar_arrive(bar(Cf::B_P_FULL + (g & 1)));
       }
@@ -820,8 +859,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       SegIter look = it;
       const bool more = kStageQ && look.next(nx);
       if (more) q_issue(p.ws.tiles[static_cast<size_t>(nx.tile) * C + rank]);
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      const float lse_v = l_run > 0.f ? m_run * p.scale + logf(l_run) : -INFINITY;
+      const float inv_l = l_run > 0.f ? p.v_scale / l_run : 0.f;
+      // l_run sums the probabilities scaled by 2^P_SHIFT
+      const float lse_v = l_run > 0.f ? m_run * p.scale + logf(l_run) - E::P_SHIFT * 0.6931471805599453f
+                                      : -INFINITY;
       if (sg.whole) {
         const int orow = td.q_row0 + t_row;
         __nv_bfloat16* dst = p.out + (static_cast<size_t>(orow) * p.Hq + td.kvh * G + g_row) * D;

@@ -180,6 +180,17 @@ __device__ __forceinline__ void umma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tm
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with e4m3 A (from TMEM) and B (shared memory): kind::f8f6f4.
+__device__ __forceinline__ void umma_e4m3_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -230,6 +241,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
   return (1u << 4)                               // D format: f32
          | (1u << 7)                             // A format: bf16
          | (1u << 10)                            // B format: bf16
+         | (static_cast<uint32_t>(a_mn) << 15)   // A major
+         | (static_cast<uint32_t>(b_mn) << 16)   // B major
+         | (static_cast<uint32_t>(N >> 3) << 17) // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);// M / 16
+}
+
+// Instruction descriptor for kind::f8f6f4 with e4m3 A/B (format code 0) and
+// an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4)                               // D format: f32
+         | (0u << 7)                             // A format: e4m3
+         | (0u << 10)                            // B format: e4m3
          | (static_cast<uint32_t>(a_mn) << 15)   // A major
          | (static_cast<uint32_t>(b_mn) << 16)   // B major
          | (static_cast<uint32_t>(N >> 3) << 17) // N / 8
@@ -402,6 +425,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two floats -> two e4m3 bytes (round to nearest, saturating at 448): lo in
+// the lower byte.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

@@ -239,3 +239,34 @@ def make_embedding(vocab: int, d_model: int, seed: int, device="cpu", dtype=torc
     ``dtype``."""
     gen = torch.Generator(device=device).manual_seed(seed)
     return _randn(gen, (vocab, d_model), device).to(dtype)
+
+
+# ------------------------------------------------------------------ e4m3 inputs
+def quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """e4m3 codes (uint8) of x / scale, clamped to the finite range +-448."""
+    return (x / scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def to_e4m3(x: torch.Tensor):
+    """(codes uint8, scale): x / scale rounded to e4m3, scale = max|x| / 448
+    (one scale per tensor, so the largest magnitude maps to the largest e4m3)."""
+    amax = float(x.abs().max())
+    scale = amax / 448.0 if amax > 0 else 1.0
+    return quantize_e4m3(x, scale), scale
+
+
+def make_fp8_batch(wl: Workload, device="cpu"):
+    """Step-0 inputs of ``wl`` for the FP8 variant: the same fp32 N(0, 1) draws
+    as ``make_batch`` (seed, order q, k, v), each tensor quantised to e4m3
+    with its own scale.  Keys q8/k8/v8 (uint8), q_scale/k_scale/v_scale and
+    the host metadata."""
+    gen = torch.Generator(device=device).manual_seed(wl.seed)
+    q = _randn(gen, (wl.total_q, wl.num_q_heads, wl.head_dim), device)
+    k = _randn(gen, (wl.total_kv, wl.num_kv_heads, wl.head_dim), device)
+    v = _randn(gen, (wl.total_kv, wl.num_kv_heads, wl.head_dim), device)
+    q8, qs = to_e4m3(q)
+    k8, ks = to_e4m3(k)
+    v8, vs = to_e4m3(v)
+    cu_q, ctx_len, mode = metadata(wl)
+    return dict(q8=q8, k8=k8, v8=v8, q_scale=qs, k_scale=ks, v_scale=vs, cu_q=cu_q,
+                ctx_len=ctx_len, mode=mode, window=wl.window, scale=wl.scale)

@@ -143,6 +143,39 @@ dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, const void* v,
                                     void* out, float* lse, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 variant: the same forward pass with Q, K and V given as e4m3 bytes (the
+ * OCP E4M3 format), one fp32 scale per tensor, so that the attention is that
+ * of q_scale * q, k_scale * k and v_scale * v.  The pages serve the model from
+ * FP8 checkpoints (agentlenshq page, "quantised checkpoints"; the throughput
+ * results are FP8 runs) but do not state FP8 attention: this is a variant.
+ *
+ * Both matrix products run on the tensor cores in e4m3 (tcgen05
+ * kind::f8f6f4) with fp32 accumulation; the softmax probabilities are scaled
+ * by 2^5 and rounded to e4m3 before P.V (relative error <= 2^-4 each), the
+ * running maximum being refreshed once it grew by more than 2^3.  out is
+ * bf16, lse fp32 (natural log of the scaled scores' exponential sum).
+ *
+ *   q  e4m3 bytes device [total_q, Hq, D]; k, v [total_kv, Hkv, D]; 16-byte aligned
+ *   head_dim 128 or 256 (64 returns DG_ERR_UNSUPPORTED)
+ *   q_scale, k_scale, v_scale  finite, > 0
+ * Everything else is as for dg_attn_forward (same workspace size).
+ */
+dg_status_t dg_attn_forward_fp8(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                                const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
+                                int32_t total_q, int32_t total_kv, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale,
+                                float q_scale, float k_scale, float v_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* dg_attn_forward_fp8 with two CUDA events recorded around the main kernel. */
+dg_status_t dg_attn_forward_fp8_profiled(
+    const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* ctx_len,
+    const uint8_t* mode, int32_t num_seqs, int32_t total_q, int32_t total_kv, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale, float q_scale,
+    float k_scale, float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+    void* stream, void* attn_begin_event, void* attn_end_event);
+
+/* ---------------------------------------------------------------------------
  * The same forward pass over a paged KV cache, with the append of the query
  * tokens' K/V fused into the call.  DiffusionGemma pages: the encoder (causal)
  * pass writes finished blocks into the KV cache and every committed canvas is
