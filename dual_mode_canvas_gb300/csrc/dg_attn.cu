@@ -249,13 +249,16 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent of the work-list grid (the kernel waits for it)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV, F8>, mk, mv, p) != cudaSuccess)
     return DG_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return DG_ERR_CUDA;

@@ -216,6 +216,9 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
                       const uint8_t* __restrict__ mode, int B, int total_q, int total_kv, int Hkv,
                       int TT, int BN, int window, int max_groups, int C, Workspace ws,
                       PagedArgs pg, int* status) {
+  // the attention kernel is launched as a programmatic dependent: its CTAs
+  // become resident while this grid runs and wait for it to finish
+  griddep_launch_dependents();
   if (blockIdx.x > 0) {
     append_rows(cu_q, ctx_len, B, total_q, pg, status);
     return;
@@ -461,6 +464,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
            const FwdParams p) {
   using Cf = FwdCfg<D, BN, NK, NV, F8>;
   using E = Elem<F8>;
+  // launched as a programmatic dependent of the work-list grid: nothing it
+  // wrote is read before that grid has finished
+  griddep_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -792,7 +798,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         // p = 2^(s * scale * log2(e) - base), two lanes per fp32x2 instruction;
         // the row sum runs in four independent fp32x2 accumulators.  With 128
         // keys per tile the MUFU ex2 rate alone would match the MMA time, so 3
-        // of every 8 pairs take the polynomial path on the FMA pipe.
+        // of every 8 pairs take the polynomial path on the FMA pipe (measured
+        // slower for the 64-key e4m3 tiles).
         constexpr int kPolyPairs = BN == 128 ? 3 : 0;
         const uint64_t sl2x2 = f32x2(sl2, sl2), nbase2 = f32x2(-base, -base);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};

@@ -80,6 +80,15 @@ __device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const void* 
       : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Dependent grid: wait until the preceding grid has completed and its writes
+// are visible.  Preceding grid: allow the dependent grid to start launching
+// (it launches once every CTA of this grid has done this or exited).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ cluster
 __device__ __forceinline__ uint32_t cluster_cta_rank() {
   uint32_t r;
