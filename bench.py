@@ -45,7 +45,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum of one main-kernel launch, from the ncu
 # capture summarised in profiles/ (kept only while the kernel is unchanged since that capture)
-NCU_TRAFFIC_BYTES = {"denoise_loop": 1.0852e9}
+NCU_TRAFFIC_BYTES = {"denoise_loop": 1.0594e9, "denoise_loop:e4m3": 9.113e7}
 
 
 def visible_pairs(wl) -> int:
@@ -384,7 +384,7 @@ def run_gpu(args):
         gbs = nbytes / (attn_avg_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(gbs / peaks["hbm_gbs"], 4)}
-    roof["traffic"] = None if paged else NCU_TRAFFIC_BYTES.get(args.workload)
+    roof["traffic"] = None if paged else NCU_TRAFFIC_BYTES.get(args.workload + (":e4m3" if fp8 else ""))
     roof["peak_source"] = f"{peaks_src} ({'sustained' if (sustained and bound == 'tensor') else 'burst'})" + (
         "; e4m3 peak = measured bf16 x 2 (nominal ratio)" if fp8 else "")
     roof["kernel"] = "fwd_kernel (persistent tcgen05 attention)"
