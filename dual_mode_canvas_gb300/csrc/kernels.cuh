@@ -106,6 +106,31 @@ struct FwdParams {
   float v_scale;            // e4m3 inputs: the v scale, applied in the epilogue (1 for bf16)
 };
 
+// Maximum of N registers by a tree of 3-input maxima: ceil(log3 N) dependent
+// levels instead of a chain of N / 2.
+template <int N>
+struct TreeMax {
+  static __device__ __forceinline__ float of(const float* v) {
+    constexpr int M = (N + 2) / 3;
+    float t[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      if (3 * i + 2 < N) t[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+      else if (3 * i + 1 < N) t[i] = fmaxf(v[3 * i], v[3 * i + 1]);
+      else t[i] = v[3 * i];
+    }
+    return TreeMax<M>::of(t);
+  }
+};
+template <>
+struct TreeMax<1> {
+  static __device__ __forceinline__ float of(const float* v) { return v[0]; }
+};
+template <>
+struct TreeMax<2> {
+  static __device__ __forceinline__ float of(const float* v) { return fmaxf(v[0], v[1]); }
+};
+
 // a row of packed P -> TMEM (16, 32 or 64 columns)
 __device__ __forceinline__ void store_packed_p(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
 __device__ __forceinline__ void store_packed_p(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
@@ -781,9 +806,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             s[c] = (key >= lo_r && key <= hi_r) ? s[c] : -INFINITY;
           }
         }
-        float mx = fmaxf(s[0], s[BN - 1]);
-#pragma unroll
-        for (int c = 1; c + 1 < BN - 1; c += 2) mx = max3f(mx, s[c], s[c + 1]);
+        // a tree of 3-input maxima (4 levels for 64 keys) instead of one chain
+        const float mx = TreeMax<BN>::of(s);
         const float m_new = fmaxf(m_run, mx);
         float m_use = m_run, alpha = 1.f;
         bool rescale = false;
