@@ -262,9 +262,18 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
   if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV, F8>, mk, mv, p) != cudaSuccess)
     return DG_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return DG_ERR_CUDA;
-  const dim3 cgrid(max_groups * p.C, (kRows + kCombineWarps - 1) / kCombineWarps);
-  combine_kernel<D><<<cgrid, kCombineWarps * 32, 0, stream>>>(p, num_clusters);
-  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  // the merge is a programmatic dependent of the attention grid (it waits
+  // for it before reading the partials)
+  cudaLaunchConfig_t ccfg = {};
+  ccfg.gridDim = dim3(max_groups * p.C, (kRows + kCombineWarps - 1) / kCombineWarps);
+  ccfg.blockDim = dim3(kCombineWarps * 32);
+  ccfg.stream = stream;
+  cudaLaunchAttribute cattr[1];
+  cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  cattr[0].val.programmaticStreamSerializationAllowed = 1;
+  ccfg.attrs = cattr;
+  ccfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&ccfg, combine_kernel<D>, p, num_clusters) != cudaSuccess) return DG_ERR_CUDA;
   return DG_OK;
 }
 

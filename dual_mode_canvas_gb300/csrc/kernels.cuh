@@ -490,8 +490,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   using Cf = FwdCfg<D, BN, NK, NV, F8>;
   using E = Elem<F8>;
   // launched as a programmatic dependent of the work-list grid: nothing it
-  // wrote is read before that grid has finished
+  // wrote is read before that grid has finished.  The split-KV merge is this
+  // grid's own dependent: it may launch at once and become resident as CTAs
+  // of this grid exit; it waits for this grid before reading the partials.
   griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -978,6 +981,9 @@ combine_kernel(const FwdParams p, int num_clusters) {
     const int cta = c * C + rank;
     return cta_unit_begin(c, U, P) >= T0 ? 2 * cta : 2 * cta + 1;
   };
+  // the partials are written by the attention grid, this grid's predecessor
+  griddep_wait();
+  // every contributor's LSE at once (lane i holds contributors i, i + 32, ...)
   float M = -INFINITY;
   for (int i = lane; i < nc; i += 32)
     M = fmaxf(M, p.ws.part_lse[static_cast<size_t>(slot_of(c_lo + i)) * kRows + r]);
@@ -988,26 +994,53 @@ combine_kernel(const FwdParams p, int num_clusters) {
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float wsum = 0.f;
-  for (int i = 0; i < nc; ++i) {
-    const int slot = slot_of(c_lo + i);
-    const float lk = p.ws.part_lse[static_cast<size_t>(slot) * kRows + r];
-    if (lk == -INFINITY) continue;
-    const float w = __expf(lk - M);
-    wsum += w;
-    const float* src = p.ws.part_o + (static_cast<size_t>(slot) * kRows + r) * D;
-    if constexpr (E % 4 == 0) {
+  for (int i0 = 0; i0 < nc; i0 += 32) {
+    // lane j: weight and slot of contributor i0 + j
+    const int cj = i0 + lane;
+    const int sj = cj < nc ? slot_of(c_lo + cj) : 0;
+    const float lj = cj < nc ? p.ws.part_lse[static_cast<size_t>(sj) * kRows + r] : -INFINITY;
+    const float wj = lj == -INFINITY ? 0.f : __expf(lj - M);
+    float ws = wj;
 #pragma unroll
-      for (int k = 0; k < E / 4; ++k) {
-        const float4 x = *reinterpret_cast<const float4*>(src + (k * 32 + lane) * 4);
-        acc[4 * k + 0] += w * x.x;
-        acc[4 * k + 1] += w * x.y;
-        acc[4 * k + 2] += w * x.z;
-        acc[4 * k + 3] += w * x.w;
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    wsum += ws;
+    const int nb = min(32, nc - i0);
+    // four contributors' rows in flight at a time
+    for (int b = 0; b < nb; b += 4) {
+      float w[4];
+      const float* src[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = min(b + u, nb - 1);
+        w[u] = b + u < nb ? __shfl_sync(0xffffffffu, wj, j) : 0.f;
+        const int sl = __shfl_sync(0xffffffffu, sj, j);
+        src[u] = p.ws.part_o + (static_cast<size_t>(sl) * kRows + r) * D;
       }
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(src + lane * 2);
-      acc[0] += w * x.x;
-      acc[1] += w * x.y;
+      if constexpr (E % 4 == 0) {
+        float4 x[4][E / 4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int k = 0; k < E / 4; ++k) x[u][k] = *reinterpret_cast<const float4*>(src[u] + (k * 32 + lane) * 4);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int k = 0; k < E / 4; ++k) {
+            acc[4 * k + 0] += w[u] * x[u][k].x;
+            acc[4 * k + 1] += w[u] * x[u][k].y;
+            acc[4 * k + 2] += w[u] * x[u][k].z;
+            acc[4 * k + 3] += w[u] * x[u][k].w;
+          }
+      } else {
+        float2 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = *reinterpret_cast<const float2*>(src[u] + lane * 2);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc[0] += w[u] * x[u].x;
+          acc[1] += w[u] * x[u].y;
+        }
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
