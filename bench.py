@@ -600,8 +600,24 @@ def run_selfcond(args):
     E = wls.make_embedding(wl.logits.vocab, wl.d_model, wl.seed, device="cuda")
     rows, vocab, d = wl.logits.rows, wl.logits.vocab, wl.d_model
     out = torch.empty((rows, d), dtype=torch.float32, device="cuda")
-    ws = torch.empty(binding.load_library().dg_selfcond_workspace_size(rows, vocab, d),
-                     dtype=torch.uint8, device="cuda")
+    lib = binding.load_library()
+    ws = torch.empty(lib.dg_sampler_workspace_size(rows, vocab, d) if args.sampler
+                     else lib.dg_selfcond_workspace_size(rows, vocab, d), dtype=torch.uint8, device="cuda")
+    if args.sampler:
+        # the whole sampler step: acceptance and self-conditioning sharing one
+        # pass of row statistics
+        _, cu_rows = wls.make_logits(wl.logits, device="cpu")
+        cu_rows = cu_rows.cuda()
+        acc_in = torch.zeros(rows, dtype=torch.uint8, device="cuda")
+        prev = torch.zeros(rows, dtype=torch.int32, device="cuda")
+        stab = torch.zeros(len(wl.logits.canvases), dtype=torch.int32, device="cuda")
+
+    def sc_call(events=None):
+        """One step; returns the self-conditioning output tensor."""
+        if args.sampler:
+            return binding.sampler_step(x, cu_rows, acc_in, prev, stab, 2.0, 3.0, 3, 0, 48, E,
+                                        workspace=ws, events=events)["selfcond"]
+        return binding.self_conditioning(x, E, out=out, workspace=ws, events=events)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     nsteps = args.warmup + args.steps
@@ -611,7 +627,7 @@ def run_selfcond(args):
             y.record(stream)
     for s_ in range(args.warmup):
         flush.fill_(s_ & 0xFF)
-        binding.self_conditioning(x, E, out=out, workspace=ws)
+        sc_call()
     torch.cuda.synchronize()
     barrier(world)
     with ClockSampler(local) as clk:
@@ -619,7 +635,7 @@ def run_selfcond(args):
             flush.fill_(s_ & 0xFF)
             e0, e1, a0, a1 = ev[s_]
             e0.record(stream)
-            binding.self_conditioning(x, E, out=out, workspace=ws, events=(a0, a1))
+            sc_call(events=(a0, a1))
             e1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -642,8 +658,7 @@ def run_selfcond(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         x.copy_(hx, non_blocking=True)
-        binding.self_conditioning(x, E, out=out, workspace=ws)
-        h_out.copy_(out, non_blocking=True)
+        h_out.copy_(sc_call(), non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         if s_ >= args.warmup:
@@ -664,17 +679,19 @@ def run_selfcond(args):
         "warmup": args.warmup, "ms_per_step": round(tot / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded logits and N(0,1) embeddings, bf16)",
-        "config": {"workload": wl.name, "rows": rows, "vocab": vocab, "d_model": d,
+        "config": {"workload": wl.name + ("+acceptance (dg_sampler_step)" if args.sampler else ""),
+                   "rows": rows, "vocab": vocab, "d_model": d,
                    "l2": "flushed before every step (256 MiB write)"},
         # row statistics, row constants, the GEMM, and the split sum when the
         # workspace holds per-split partials (beyond the statistics)
-        "gpu_launches": (4 if ws.numel() > _a256(16 * rows * -(-(vocab + (7 if vocab % 8 else 0)) // 16384))
-                         + _a256(4 * rows) else 3) * args.steps * world,
+        "gpu_launches": ((4 if ws.numel() > _a256(16 * rows * -(-(vocab + (7 if vocab % 8 else 0)) // 16384))
+                          + _a256(4 * rows) else 3) + (1 if args.sampler else 0)) * args.steps * world,
         "roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "achieved": round(ktf, 2),
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": round(ktf / tc_peak, 4),
                      "traffic": None,
                      "peak_source": f"{src} ({'sustained' if sustained else 'burst'})",
-                     "kernel": "sc_kernel (persistent tcgen05 softmax x E)",
+                     "kernel": ("dg_sampler_step, whole call (events around the call)" if args.sampler
+                                else "sc_kernel (persistent tcgen05 softmax x E)"),
                      "kernel_ms_per_launch": round(kavg, 4),
                      "tighter_roof_frac": round(max(t_tc, t_hbm) / (kavg * 1e-3), 4)},
         "clocks": clk.summary(),
@@ -708,6 +725,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--fp8", action="store_true",
                     help="run the attention in e4m3 (Q, K, V codes with one scale per tensor)")
+    ap.add_argument("--sampler", action="store_true",
+                    help="self-conditioning workloads: time the combined sampler step (acceptance + "
+                         "self-conditioning sharing one statistics pass)")
     ap.add_argument("--paged", type=int, default=0,
                     help="page size: run the step through the paged KV cache (0: contiguous)")
     ap.add_argument("--workload", default="denoise_loop",

@@ -30,7 +30,8 @@ EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profil
             "dg_attn_forward_noalloc", "dg_attn_forward_paged", "dg_attn_forward_paged_profiled",
             "dg_attn_forward_fp8", "dg_attn_forward_fp8_profiled",
             "dg_selfcond_workspace_size", "dg_selfcond_forward", "dg_selfcond_forward_profiled",
-            "dg_accept_workspace_size", "dg_accept_step",
+            "dg_accept_workspace_size", "dg_accept_step", "dg_sampler_workspace_size",
+            "dg_sampler_step",
             "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
 
 _lib = None
@@ -90,6 +91,11 @@ def load_library():
     lib.dg_accept_step.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, f32, f32, i32, i32, i32,
                                    vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.dg_accept_step.restype = ctypes.c_int
+    lib.dg_sampler_workspace_size.argtypes = [i32, i32, i32]
+    lib.dg_sampler_workspace_size.restype = sz
+    lib.dg_sampler_step.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, f32, f32, i32, i32, i32, vp, i32,
+                                    vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.dg_sampler_step.restype = ctypes.c_int
     lib.dg_attn_status.argtypes = [vp]
     lib.dg_attn_status.restype = ctypes.c_int
     lib.dg_attn_error_string.argtypes = [i32]
@@ -341,4 +347,53 @@ def accept_step(logits, cu_rows, accepted_in, argmax_prev, stable_in, entropy_bu
         events[1].record(torch.cuda.current_stream() if stream is None else stream)
     if rc != DG_OK:
         raise DgAttnError(rc, "dg_accept_step")
+    return res
+
+
+def sampler_step(logits, cu_rows, accepted_in, argmax_prev, stable_in, entropy_budget: float,
+                 entropy_threshold: float, patience: int, step: int, max_steps: int, embedding, *,
+                 workspace=None, stream=None, events=None):
+    """Acceptance step and self-conditioning average of one step's logits
+    through ``dg_sampler_step`` (one pass of row statistics for both).
+    Returns the ``accept_step`` dict plus ``selfcond`` [rows, d_model] fp32.
+    ``events=(begin, end)`` are recorded around the call on the stream."""
+    lib = load_library()
+    for name, t, dt in (("logits", logits, torch.bfloat16), ("cu_rows", cu_rows, torch.int32),
+                        ("accepted_in", accepted_in, torch.uint8),
+                        ("argmax_prev", argmax_prev, torch.int32), ("stable_in", stable_in, torch.int32),
+                        ("embedding", embedding, torch.bfloat16)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    rows, vocab = logits.shape
+    d = embedding.shape[1]
+    if embedding.shape[0] != vocab:
+        raise ValueError("embedding must be [vocab, d_model]")
+    nb = cu_rows.numel() - 1
+    dev = logits.device
+    res = dict(entropy=torch.empty(rows, dtype=torch.float32, device=dev),
+               confidence=torch.empty(rows, dtype=torch.float32, device=dev),
+               argmax=torch.empty(rows, dtype=torch.int32, device=dev),
+               accepted=torch.empty(rows, dtype=torch.uint8, device=dev),
+               stable=torch.empty(nb, dtype=torch.int32, device=dev),
+               converged=torch.empty(nb, dtype=torch.uint8, device=dev),
+               selfcond=torch.empty((rows, d), dtype=torch.float32, device=dev))
+    need = lib.dg_sampler_workspace_size(rows, vocab, d)
+    if need == 0:
+        raise DgAttnError(DG_ERR_INVALID_ARG, "dg_sampler_workspace_size")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    sh = _stream_handle(stream)
+    if events is not None:
+        events[0].record(torch.cuda.current_stream() if stream is None else stream)
+    rc = lib.dg_sampler_step(_ptr(logits), rows, vocab, _ptr(cu_rows), nb, _ptr(accepted_in),
+                             _ptr(argmax_prev), _ptr(stable_in), float(entropy_budget),
+                             float(entropy_threshold), int(patience), int(step), int(max_steps),
+                             _ptr(embedding), d, _ptr(res["entropy"]), _ptr(res["confidence"]),
+                             _ptr(res["argmax"]), _ptr(res["accepted"]), _ptr(res["stable"]),
+                             _ptr(res["converged"]), _ptr(res["selfcond"]), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), sh)
+    if events is not None:
+        events[1].record(torch.cuda.current_stream() if stream is None else stream)
+    if rc != DG_OK:
+        raise DgAttnError(rc, "dg_sampler_step")
     return res

@@ -613,9 +613,11 @@ bool sc_shapes_ok(int32_t rows, int32_t vocab, int32_t d) {
   return rows >= 1 && vocab >= 8 && vocab % 8 == 0 && d >= 8 && d % 8 == 0;
 }
 
+// stats_ready: the row statistics of these logits are already at the
+// workspace's start (written by the acceptance step of the same call)
 dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const void* embedding,
                           int32_t d_model, float* out, void* workspace, size_t workspace_bytes,
-                          void* stream_ptr, void* ev_begin, void* ev_end) {
+                          void* stream_ptr, void* ev_begin, void* ev_end, bool stats_ready = false) {
   if (!sc_shapes_ok(rows, vocab, d_model)) return DG_ERR_INVALID_ARG;
   if (!logits || !embedding || !out || !aligned(logits, 16) || !aligned(embedding, 16) ||
       !aligned(out, 16))
@@ -654,8 +656,9 @@ dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const
   p.kblocks = pl.kblocks;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  row_stats_kernel<<<static_cast<unsigned>(rows) * pl.chunks, kStatThreads, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(logits), vocab, pl.chunks, stats);
+  if (!stats_ready)
+    row_stats_kernel<<<static_cast<unsigned>(rows) * pl.chunks, kStatThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(logits), vocab, pl.chunks, stats);
   sc_rowconst_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(stats, rows, pl.chunks,
                                                          const_cast<float*>(p.rowc));
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
@@ -794,3 +797,38 @@ extern "C" const char* dg_attn_error_string(int32_t status) {
 }
 
 extern "C" int32_t dg_attn_version(void) { return kVersion; }
+
+// The sampler's work on one denoise step's logits in one call: the acceptance
+// step and the self-conditioning average share one pass of row statistics.
+extern "C" size_t dg_sampler_workspace_size(int32_t rows, int32_t vocab, int32_t d_model) {
+  const size_t a = dg_accept_workspace_size(rows, vocab);
+  const size_t b = dg_selfcond_workspace_size(rows, vocab, d_model);
+  if (a == 0 || b == 0) return 0;
+  return a > b ? a : b;
+}
+
+extern "C" dg_status_t dg_sampler_step(const void* logits, int32_t rows, int32_t vocab,
+                                       const int32_t* cu_rows, int32_t num_canvases,
+                                       const uint8_t* accepted_in, const int32_t* argmax_prev,
+                                       const int32_t* stable_in, float entropy_budget,
+                                       float entropy_threshold, int32_t patience, int32_t step,
+                                       int32_t max_steps, const void* embedding, int32_t d_model,
+                                       float* entropy_out, float* confidence_out,
+                                       int32_t* argmax_out, uint8_t* accepted_out,
+                                       int32_t* stable_out, uint8_t* converged_out,
+                                       float* selfcond_out, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  if (rows == 0) return num_canvases >= 0 ? DG_OK : DG_ERR_INVALID_ARG;
+  if (num_canvases < 1 || !sc_shapes_ok(rows, vocab, d_model)) return DG_ERR_INVALID_ARG;
+  if (!embedding || !selfcond_out || !aligned(embedding, 16) || !aligned(selfcond_out, 16))
+    return DG_ERR_INVALID_ARG;
+  if (workspace_bytes < dg_sampler_workspace_size(rows, vocab, d_model)) return DG_ERR_WORKSPACE;
+  const dg_status_t st = dg_accept_step(logits, rows, vocab, cu_rows, num_canvases, accepted_in,
+                                        argmax_prev, stable_in, entropy_budget, entropy_threshold,
+                                        patience, step, max_steps, entropy_out, confidence_out,
+                                        argmax_out, accepted_out, stable_out, converged_out,
+                                        workspace, workspace_bytes, stream);
+  if (st != DG_OK) return st;
+  return selfcond_impl(logits, rows, vocab, embedding, d_model, selfcond_out, workspace,
+                       workspace_bytes, stream, nullptr, nullptr, true);
+}

@@ -311,6 +311,29 @@ dg_status_t dg_accept_step(const void* logits, int32_t rows, int32_t vocab,
                            uint8_t* accepted_out, int32_t* stable_out, uint8_t* converged_out,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * The sampler's per-step work on one set of LM-head logits, in one call: the
+ * acceptance step above and the self-conditioning average (dg_selfcond_forward)
+ * of the same logits (DiffusionGemma, agentlenshq page, "sampling loop and
+ * entropy-bounded denoising" and "self-conditioning for stability": both are
+ * taken from the same step's softmax distribution).  Both need every row's softmax statistics; they are
+ * computed once (one pass over the logits instead of two).  Arguments as in
+ * the two calls; workspace >= dg_sampler_workspace_size(rows, vocab, d_model)
+ * bytes, 256-byte aligned.  The outputs equal those of the two separate calls
+ * bit for bit.
+ */
+size_t dg_sampler_workspace_size(int32_t rows, int32_t vocab, int32_t d_model);
+
+dg_status_t dg_sampler_step(const void* logits, int32_t rows, int32_t vocab, const int32_t* cu_rows,
+                            int32_t num_canvases, const uint8_t* accepted_in,
+                            const int32_t* argmax_prev, const int32_t* stable_in,
+                            float entropy_budget, float entropy_threshold, int32_t patience,
+                            int32_t step, int32_t max_steps, const void* embedding, int32_t d_model,
+                            float* entropy_out, float* confidence_out, int32_t* argmax_out,
+                            uint8_t* accepted_out, int32_t* stable_out, uint8_t* converged_out,
+                            float* selfcond_out, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* Synchronises `stream`, returns the current device's status word (DG_OK if
  * no device-side error was recorded since the last call) and clears it. */
 dg_status_t dg_attn_status(void* stream);

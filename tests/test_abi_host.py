@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dg_(?:attn|accept|selfcond)_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(dg_(?:attn|accept|selfcond|sampler)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_abi():
