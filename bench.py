@@ -309,6 +309,7 @@ def run_gpu(args):
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
+    torch.cuda.nvtx.range_push("timed steps")
     with ClockSampler(local) as clk:
         for s in range(args.warmup, nsteps):
             stage(s)
@@ -317,6 +318,7 @@ def run_gpu(args):
             call(events=(a0, a1))
             e1.record(stream)
         torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier(world)
     t_wall = time.perf_counter() - t_wall0
     st = binding.status()

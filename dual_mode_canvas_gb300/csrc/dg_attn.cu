@@ -11,6 +11,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "dg_attn.h"
 #include "kernels.cuh"
 #include "acceptance.cuh"
@@ -46,6 +48,15 @@ struct DeviceInfo {
 };
 
 std::mutex g_mutex;
+
+// An NVTX range around each C-ABI call (header-only NVTX: free unless a
+// profiler is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -408,6 +419,7 @@ extern "C" dg_status_t dg_attn_forward(const void* q, const void* k, const void*
                                        int32_t head_dim, int32_t window, float scale, void* out,
                                        float* lse, void* workspace, size_t workspace_bytes,
                                        void* stream) {
+  NvtxRange nvtx("dg_attn_forward");
   return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
                       num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
                       stream, nullptr, nullptr);
@@ -419,6 +431,7 @@ extern "C" dg_status_t dg_attn_forward_profiled(
     int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale, void* out, float* lse,
     void* workspace, size_t workspace_bytes, void* stream, void* attn_begin_event,
     void* attn_end_event) {
+  NvtxRange nvtx("dg_attn_forward_profiled");
   return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
                       num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
                       stream, attn_begin_event, attn_end_event);
@@ -433,6 +446,7 @@ extern "C" dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, con
                                                int32_t num_q_heads, int32_t num_kv_heads,
                                                int32_t head_dim, int32_t window, float scale,
                                                void* out, float* lse, void* stream) {
+  NvtxRange nvtx("dg_attn_forward_noalloc");
   if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim) || num_seqs == 0 ||
       total_q == 0)
     return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
@@ -473,6 +487,7 @@ extern "C" dg_status_t dg_attn_forward_fp8(const void* q, const void* k, const v
                                            float scale, float q_scale, float k_scale, float v_scale,
                                            void* out, float* lse, void* workspace,
                                            size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx("dg_attn_forward_fp8");
   return forward_fp8(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
                      num_kv_heads, head_dim, window, scale, q_scale, k_scale, v_scale, out, lse,
                      workspace, workspace_bytes, stream, nullptr, nullptr);
@@ -484,6 +499,7 @@ extern "C" dg_status_t dg_attn_forward_fp8_profiled(
     int32_t num_kv_heads, int32_t head_dim, int32_t window, float scale, float q_scale,
     float k_scale, float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
     void* stream, void* attn_begin_event, void* attn_end_event) {
+  NvtxRange nvtx("dg_attn_forward_fp8_profiled");
   return forward_fp8(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
                      num_kv_heads, head_dim, window, scale, q_scale, k_scale, v_scale, out, lse,
                      workspace, workspace_bytes, stream, attn_begin_event, attn_end_event);
@@ -534,6 +550,7 @@ extern "C" dg_status_t dg_attn_forward_paged(
     const int32_t* cu_q, const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
     int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t window,
     float scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx("dg_attn_forward_paged");
   return forward_paged(q, k_new, v_new, k_cache, v_cache, num_pages, page_size, block_table,
                        max_pages_per_seq, cu_q, ctx_len, mode, num_seqs, total_q, num_q_heads,
                        num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
@@ -547,6 +564,7 @@ extern "C" dg_status_t dg_attn_forward_paged_profiled(
     int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t window,
     float scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream,
     void* attn_begin_event, void* attn_end_event) {
+  NvtxRange nvtx("dg_attn_forward_paged_profiled");
   return forward_paged(q, k_new, v_new, k_cache, v_cache, num_pages, page_size, block_table,
                        max_pages_per_seq, cu_q, ctx_len, mode, num_seqs, total_q, num_q_heads,
                        num_kv_heads, head_dim, window, scale, out, lse, workspace, workspace_bytes,
@@ -698,6 +716,7 @@ extern "C" size_t dg_selfcond_workspace_size(int32_t rows, int32_t vocab, int32_
 extern "C" dg_status_t dg_selfcond_forward(const void* logits, int32_t rows, int32_t vocab,
                                            const void* embedding, int32_t d_model, float* out,
                                            void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx("dg_selfcond_forward");
   return selfcond_impl(logits, rows, vocab, embedding, d_model, out, workspace, workspace_bytes,
                        stream, nullptr, nullptr);
 }
@@ -707,6 +726,7 @@ extern "C" dg_status_t dg_selfcond_forward_profiled(const void* logits, int32_t 
                                                     int32_t d_model, float* out, void* workspace,
                                                     size_t workspace_bytes, void* stream,
                                                     void* gemm_begin_event, void* gemm_end_event) {
+  NvtxRange nvtx("dg_selfcond_forward_profiled");
   return selfcond_impl(logits, rows, vocab, embedding, d_model, out, workspace, workspace_bytes,
                        stream, gemm_begin_event, gemm_end_event);
 }
@@ -726,6 +746,7 @@ extern "C" dg_status_t dg_accept_step(const void* logits, int32_t rows, int32_t 
                                       int32_t* argmax_out, uint8_t* accepted_out,
                                       int32_t* stable_out, uint8_t* converged_out, void* workspace,
                                       size_t workspace_bytes, void* stream_ptr) {
+  NvtxRange nvtx("dg_accept_step");
   if (rows < 0 || vocab < 1 || num_canvases < 0 || patience < 0 || max_steps < 1 || step < 0 ||
       !std::isfinite(entropy_budget) || entropy_budget < 0.f || !std::isfinite(entropy_threshold))
     return DG_ERR_INVALID_ARG;
@@ -818,6 +839,7 @@ extern "C" dg_status_t dg_sampler_step(const void* logits, int32_t rows, int32_t
                                        int32_t* stable_out, uint8_t* converged_out,
                                        float* selfcond_out, void* workspace,
                                        size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx("dg_sampler_step");
   if (rows == 0) return num_canvases >= 0 ? DG_OK : DG_ERR_INVALID_ARG;
   if (num_canvases < 1 || !sc_shapes_ok(rows, vocab, d_model)) return DG_ERR_INVALID_ARG;
   if (!embedding || !selfcond_out || !aligned(embedding, 16) || !aligned(selfcond_out, 16))
