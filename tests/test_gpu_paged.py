@@ -4,6 +4,8 @@ seeded inputs: attention outputs within the attention bar, the cache after the
 append bit for bit, and the paged result bit-identical to the contiguous path
 on the same keys."""
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -79,9 +81,21 @@ def _bits(t):
     return t.cpu().view(torch.int16).numpy()
 
 
-def test_paged_equals_contiguous_bit_for_bit():
+@pytest.mark.parametrize("cluster", ["2", "4"])
+def test_paged_equals_contiguous_bit_for_bit(cluster):
     """The same keys laid out contiguously (gathered through the page table by
-    the oracle's gather) give bit-identical outputs through dg_attn_forward."""
+    the oracle's gather) give bit-identical outputs through dg_attn_forward,
+    with both calls in the same launch configuration (the default cluster size
+    of a paged call depends on the page size, and a different split of the
+    work changes the rounding order)."""
+    os.environ["DG_ATTN_CLUSTER"] = cluster
+    try:
+        _paged_vs_contiguous()
+    finally:
+        del os.environ["DG_ATTN_CLUSTER"]
+
+
+def _paged_vs_contiguous():
     wl = wls.Workload("paged", ((300, 256, 1), (0, 333, 0), (1000, 200, 1)), 8, 4, 128, -1, 77)
     b = wls.make_paged_batch(wl, 16, device="cuda")
     d = to_dev(b)
