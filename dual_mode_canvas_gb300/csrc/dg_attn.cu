@@ -178,9 +178,12 @@ dg_status_t device_info(DeviceInfo** out) {
 // TMA box: a larger cluster gives each CTA a shorter slice, so fewer boxes,
 // and shares each of them more widely (measured on 16-row pages and 128-key
 // tiles: clusters of 4 take 1.02 ms where clusters of 2 take 1.14 ms and the
-// contiguous layout 0.98 ms; for the contiguous layout 2 is best).
+// contiguous layout 0.98 ms).  Contiguous K/V with the rotated KV order (most
+// reads are L2 hits, so multicast saves little): head_dim 128 runs best in
+// pairs (max mix 1.019 vs 1.028 ms per step unpaired), head_dim 256 unpaired
+// (denoise step 0.242 vs 0.247 ms in pairs; e4m3 0.196 vs 0.205 ms).
 int cluster_for(const DeviceInfo& di, int D, bool f8 = false, int page_size = 0) {
-  int C = 2;
+  int C = D == 256 ? 1 : 2;
   if (page_size > 0) {
     const int BN = kv_tile_rows(D, f8);
     if (page_size * 2 < BN) C = std::min(4, std::max(2, BN / (2 * page_size)));
@@ -191,6 +194,13 @@ int cluster_for(const DeviceInfo& di, int D, bool f8 = false, int page_size = 0)
   }
   while (C > 1 && di.max_clusters[f8 ? 1 : 0][dim_slot(D)][cluster_slot(C)] < 1) C >>= 1;
   return C;
+}
+
+// Each group's KV tiles are visited in the rotated order that lines up the
+// clusters streaming the same KV (DG_ATTN_KV_ORDER=linear: ascending order).
+bool rotate_kv_order() {
+  const char* e = std::getenv("DG_ATTN_KV_ORDER");
+  return !(e && std::strcmp(e, "linear") == 0);
 }
 
 // Persistent grid: as many clusters as are co-resident (DG_ATTN_NUM_CTAS caps
@@ -403,11 +413,11 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
       append_ctas = static_cast<int>(std::min<int64_t>((units + 1023) / 1024, 2ll * di->num_sms));
     }
   }
+  const int num_clusters = num_clusters_for(*di, head_dim, Ccl, f8);
   build_worklist_kernel<<<1 + append_ctas, 1024, 0, stream>>>(
       cu_q, ctx_len, mode, num_seqs, total_q, pg ? INT32_MAX : total_kv, num_kv_heads, TT, BN,
-      window, lay.max_tiles, Ccl, p.ws, pa, p.status);
+      window, lay.max_tiles, Ccl, num_clusters, rotate_kv_order() ? 1 : 0, p.ws, pa, p.status);
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
-  const int num_clusters = num_clusters_for(*di, head_dim, Ccl, f8);
   cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
   if (f8) {
     if (head_dim == 128) return launch<128, true>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);

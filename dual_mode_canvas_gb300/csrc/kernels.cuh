@@ -70,7 +70,16 @@ struct TileDesc {
   int32_t kt_first;  // first KV tile of the group's range (units of BN keys, sequence-relative)
   int32_t kvh;       // KV head
   int32_t causal;    // 1 causal (encoder), 0 bidirectional (denoise)
+  int32_t kt_count;  // KV tiles in the group's range
+  int32_t kt_rot;    // the group's KV tiles are visited from kt_first + kt_rot on, cyclically
 };
+
+// KV tile (sequence-relative, units of BN keys) visited j-th in a group.
+__device__ __forceinline__ int kv_tile(const TileDesc& td, int j) {
+  int x = j + td.kt_rot;
+  if (x >= td.kt_count) x -= td.kt_count;
+  return td.kt_first + x;
+}
 
 struct WorkHeader {
   int32_t num_tiles;  // tile groups (one per cluster-wide work item)
@@ -234,13 +243,33 @@ __device__ void append_rows(const int32_t* __restrict__ cu_q, const int32_t* __r
   }
 }
 
+// --------------------------------------------------------- work splitting
+// The U work units are cut into P = min(grid, U) contiguous CTA ranges, so no
+// CTA range is empty.
+__device__ __forceinline__ int active_ctas(int grid, int64_t U) {
+  return U < grid ? static_cast<int>(U) : grid;
+}
+
+__device__ __forceinline__ int64_t cta_unit_begin(int c, int64_t U, int P) {
+  return static_cast<int64_t>(c) * U / P;
+}
+
+// CTA whose unit range contains unit u (ranges are [begin(c), begin(c+1))).
+__device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int P) {
+  int c = static_cast<int>((u * P) / U);
+  if (c > P - 1) c = P - 1;
+  while (c + 1 < P && cta_unit_begin(c + 1, U, P) <= u) ++c;
+  while (c > 0 && cta_unit_begin(c, U, P) > u) --c;
+  return c;
+}
+
 // ------------------------------------------------------ work-list builder
 // CTA 0 builds the work list; with a paged cache, CTAs 1.. append the new K/V.
 __global__ void __launch_bounds__(1024, 1)
 build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ ctx_len,
                       const uint8_t* __restrict__ mode, int B, int total_q, int total_kv, int Hkv,
-                      int TT, int BN, int window, int max_groups, int C, Workspace ws,
-                      PagedArgs pg, int* status) {
+                      int TT, int BN, int window, int max_groups, int C, int num_clusters,
+                      int rotate, Workspace ws, PagedArgs pg, int* status) {
   // the attention kernel is launched as a programmatic dependent: its CTAs
   // become resident while this grid runs and wait for it to finish
   griddep_launch_dependents();
@@ -332,6 +361,8 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
       td.kt_first = kv_lo / BN;
       td.kvh = kvh;
       td.causal = causal ? 1 : 0;
+      td.kt_count = kv_hi / BN - kv_lo / BN + 1;
+      td.kt_rot = 0;
       ws.tiles[static_cast<size_t>(grp) * C + r] = td;
     }
     ws.unit_begin[grp] = kSegWeight + kv_hi / BN - kv_lo / BN + 1;
@@ -343,26 +374,26 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     ws.hdr->total_units = ws.unit_begin[num_tiles];
     ws.hdr->error = 0;
   }
-}
-
-// --------------------------------------------------------- work splitting
-// The U work units are cut into P = min(grid, U) contiguous CTA ranges, so no
-// CTA range is empty.
-__device__ __forceinline__ int active_ctas(int grid, int64_t U) {
-  return U < grid ? static_cast<int>(U) : grid;
-}
-
-__device__ __forceinline__ int64_t cta_unit_begin(int c, int64_t U, int P) {
-  return static_cast<int64_t>(c) * U / P;
-}
-
-// CTA whose unit range contains unit u (ranges are [begin(c), begin(c+1))).
-__device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int P) {
-  int c = static_cast<int>((u * P) / U);
-  if (c > P - 1) c = P - 1;
-  while (c + 1 < P && cta_unit_begin(c + 1, U, P) <= u) ++c;
-  while (c > 0 && cta_unit_begin(c, U, P) > u) --c;
-  return c;
+  if (!rotate) return;
+  // KV visiting order.  The clusters' unit ranges are contiguous and equally
+  // long (U / P units), so the clusters sharing one group start at KV-tile
+  // offsets a multiple of U / P apart.  Rotating each group's tiles so that
+  // the cluster holding its first tile reaches that tile at "time" (units
+  // since the launch) equal to the tile index gives every cluster of every
+  // group a phase that is a multiple of U / P: the groups of one (sequence,
+  // KV head) with the same KV range then stream the same KV tiles at about
+  // the same time, and the later readers find them in L2.  The order of the
+  // tiles does not change the result beyond fp32 rounding.
+  const int64_t U = ws.unit_begin[num_tiles];
+  const int P = active_ctas(num_clusters, U);
+  for (int grp = tid; grp < num_tiles; grp += 1024) {
+    const int64_t r0 = ws.unit_begin[grp] + kSegWeight;
+    const int64_t n = ws.unit_begin[grp + 1] - r0;
+    if (n <= 1 || P <= 1) continue;
+    const int64_t lead = r0 - cta_unit_begin(cta_of_unit(r0, U, P), U, P);  // >= 0
+    const int rot = static_cast<int>(lead % n);
+    for (int r = 0; r < C; ++r) ws.tiles[static_cast<size_t>(grp) * C + r].kt_rot = rot;
+  }
 }
 
 // Tile containing unit u: largest t with unit_begin[t] <= u.
@@ -610,7 +641,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           mbar_arrive_expect_tx(full0 + 8u * stage, t_tx);
           const uint32_t dst = ring + stage * Cf::KV_BYTES + rank * slice * 128;
           if (p.block_table == nullptr) {
-            const int row = td.kv_row0 + (td.kt_first + j) * BN + rank * slice;
+            const int row = td.kv_row0 + kv_tile(td, j) * BN + rank * slice;
 #pragma unroll
             for (int kb = 0; kb < Cf::NKB; ++kb) {
               if (C > 1)
@@ -622,7 +653,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           } else {
             // positions past the sequence's last key read its last page
             // (checked by the work-list launch); the softmax masks them
-            const int pos0 = (td.kt_first + j) * BN + rank * slice;
+            const int pos0 = kv_tile(td, j) * BN + rank * slice;
             const int last_page = (td.L - 1) >> p.page_shift;
             const int pmask = (1 << p.page_shift) - 1;
             for (int r0 = 0; r0 < slice; r0 += p.page_box) {
@@ -791,7 +822,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       const int n = sg.j1 - sg.j0;
       for (int jj = 0; jj < n; ++jj) {
         const uint32_t g = gj + jj;
-        const int kv0 = (td.kt_first + sg.j0 + jj) * BN;
+        const int kv0 = kv_tile(td, sg.j0 + jj) * BN;
         if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_S_FULL + (g & 1)), (g >> 1) & 1, abort_flag, p.status))) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[BN];

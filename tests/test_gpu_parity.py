@@ -173,6 +173,18 @@ def test_causal_row0_without_context_is_exact():
     assert torch.equal(out[0], dev["v"][0])
 
 
+def lse_order_bound(lse_a, lse_b, max_keys, bn=128):
+    """How far two LSEs of the same rows may differ when the kernel visits the
+    KV tiles in another order or cuts them elsewhere.  The row sum l runs over
+    T = ceil(keys / BN) tiles: each tile adds one fp32 rounding (2^-24) and,
+    when its maximum grows, one rescale by an ex2 approximation (2^-22
+    relative), so each side's l is within T (2^-22 + 2^-24) of the exact sum;
+    the LSE adds ln l and a few ulps of its own value."""
+    T = -(-max_keys // bn)
+    ulp = torch.maximum(lse_a.abs(), lse_b.abs()) * 2.0 ** -23
+    return 2 * T * (2.0 ** -22 + 2.0 ** -24) + 4 * ulp
+
+
 def test_split_kv_matches_single_cta():
     """The LSE merge of split tiles equals the unsplit result (fp32 rounding)."""
     wl, batch = wls.random_batch(9, ((3000, 256, 1), (1000, 300, 0)), 8, 2, 128, -1)
@@ -184,7 +196,29 @@ def test_split_kv_matches_single_cta():
     finally:
         del os.environ["DG_ATTN_NUM_CTAS"]
     assert (out_split.float() - out_one.float()).abs().max().item() <= 2 ** -7
-    assert (lse_split - lse_one).abs().max().item() <= 1e-5
+    assert ((lse_split - lse_one).abs() <= lse_order_bound(lse_split, lse_one, 3256)).all()
+
+
+@pytest.mark.parametrize("ctas", ["152", "10"])
+def test_rotated_kv_order_matches_ascending(ctas):
+    """Visiting each group's KV tiles from a rotated start (the default) gives
+    the ascending-order result up to fp32 rounding, with the cut points of the
+    full grid and of a 10-CTA grid (many cuts inside each group)."""
+    wl, batch = wls.random_batch(10, ((3000, 256, 1), (1000, 300, 0), (500, 64, 1)), 8, 2, 128, -1)
+    dev = to_dev(batch)
+    os.environ["DG_ATTN_NUM_CTAS"] = ctas
+    try:
+        for W in (-1, 700):
+            out_rot, lse_rot = run_gpu(dev, W, wl.scale)
+            os.environ["DG_ATTN_KV_ORDER"] = "linear"
+            try:
+                out_lin, lse_lin = run_gpu(dev, W, wl.scale)
+            finally:
+                del os.environ["DG_ATTN_KV_ORDER"]
+            assert (out_rot.float() - out_lin.float()).abs().max().item() <= 2 ** -7, W
+            assert ((lse_rot - lse_lin).abs() <= lse_order_bound(lse_rot, lse_lin, 3256)).all(), W
+    finally:
+        del os.environ["DG_ATTN_NUM_CTAS"]
 
 
 def test_device_detected_bad_metadata_sets_status():
