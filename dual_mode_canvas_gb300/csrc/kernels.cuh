@@ -468,6 +468,33 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Waits for the P and V of one PV together and, in the same rounds, tests the
+// K stage of the next QK^T.  Each mbarrier test costs the MMA warp ~130 clocks
+// of latency; the three are independent, so one round costs about one test.
+__device__ __forceinline__ bool wait_pv_probe_k(uint32_t pbar, uint32_t pparity, uint32_t vbar,
+                                                uint32_t vparity, uint32_t kbar, uint32_t kparity,
+                                                bool& k_ready, volatile int* abort_flag, int* status) {
+  bool p_ok = false, v_ok = false;
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    const bool tp = mbar_test_wait(pbar, pparity);
+    const bool tv = mbar_test_wait(vbar, vparity);
+    const bool tk = mbar_test_wait(kbar, kparity);
+    p_ok = p_ok || tp;
+    v_ok = v_ok || tv;
+    k_ready = k_ready || tk;
+    if (p_ok && v_ok) return true;
+    if (*abort_flag) return false;
+    if (it == 0) {
+      t0 = global_timer_ns();
+    } else if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      record_error(status, kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // -------------------------------------------------------------- main kernel
 // Element type of Q, K, V and of P: bf16 (tcgen05 kind::f16) or e4m3
 // (kind::f8f6f4).  Sizes in elements of the 128-byte swizzle block, of one
@@ -546,6 +573,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   const int64_t u_beg = cta_unit_begin(cl, U, P);
   const int64_t u_end = cta_unit_begin(cl + 1, U, P);
   const uint16_t cta_mask = static_cast<uint16_t>((1u << C) - 1u);
+  // K / V stages released by a softmax thread (see the MMA issuer) or by
+  // tcgen05.commit from the MMA warp
+  const bool soft_release = (BN == 64) && (C == 1);
 
   const uint32_t sK = sbase + Cf::OFF_K;
   const uint32_t sV = sbase + Cf::OFF_V;
@@ -556,7 +586,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Cf::B_Q_FULL), kRows);
-    // a K/V slot is free once every CTA of the cluster has consumed it
+    // a K/V slot is free once every CTA of the cluster has consumed it: C
+    // commits from the MMA warps, or (soft_release, C == 1) one softmax arrive
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(Cf::B_K_FULL + s), 1);
       mbar_init(bar(Cf::B_K_EMPTY + s), C);
@@ -691,6 +722,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // as PV(g) has been issued.  The whole warp runs this loop with identical
     // (warp-uniform) operands and one elected lane issues each tcgen05 op:
     // issuing from a single divergent lane cost ~100 clocks per MMA.
+    //
+    // This warp's loop sets the pace: every mbarrier test and every commit
+    // costs it 100-300 clocks, against ~1000 clocks of MMAs per tile.  So it
+    // tests P, V and the next K together, and, where the softmax warps have
+    // time to spare (64-key tiles, no cluster), leaves the release of the K
+    // and V stages to them (soft_release) instead of committing to the empty
+    // barriers itself.
     {
       constexpr uint32_t idesc_qk = F8 ? idesc_e4m3_f32(kRows, BN, 0, 0) : idesc_bf16_f32(kRows, BN, 0, 0);
       constexpr uint32_t idesc_pv = F8 ? idesc_e4m3_f32(kRows, D, 0, 1) : idesc_bf16_f32(kRows, D, 0, 1);
@@ -698,6 +736,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       uint32_t gj = 0;
       int seg_i = 0;
       bool ok = true;
+      bool k_ready = false;  // the next QK's K stage was seen full by the last probe
       Seg sg;
       while (ok && it.next(sg)) {
         if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_Q_FULL), seg_i & 1, abort_flag, p.status))) { ok = false; break; }
@@ -706,7 +745,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         for (int jj = 0; jj <= n && ok; ++jj) {
           if (jj < n) {
             const uint32_t g = gj + jj;
-            if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_K_FULL + k_stage), k_phase, abort_flag, p.status))) { ok = false; break; }
+            if (!k_ready &&
+                !__all_sync(0xffffffffu, wait_phase(bar(Cf::B_K_FULL + k_stage), k_phase, abort_flag, p.status))) { ok = false; break; }
+            k_ready = false;
             tc_fence_after();
             const uint32_t d_s = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
             const uint32_t k_base = sK + k_stage * Cf::KV_BYTES;
@@ -717,8 +758,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
               else umma_bf16_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
             }
             umma_commit_warp(bar(Cf::B_S_FULL + (g & 1)));
-            if (C > 1) umma_commit_multicast_warp(bar(Cf::B_K_EMPTY + k_stage), cta_mask);
-            else umma_commit_warp(bar(Cf::B_K_EMPTY + k_stage));
+            if (!soft_release) {
+              if (C > 1) umma_commit_multicast_warp(bar(Cf::B_K_EMPTY + k_stage), cta_mask);
+              else umma_commit_warp(bar(Cf::B_K_EMPTY + k_stage));
+            }
             if (++k_stage == NK) { k_stage = 0; k_phase ^= 1; }
           }
           if (jj >= 1) {
@@ -726,8 +769,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             const bool first = (jj == 1);
             if (first && seg_i > 0 &&
                 !__all_sync(0xffffffffu, wait_phase(bar(Cf::B_O_FREE), (seg_i - 1) & 1, abort_flag, p.status))) { ok = false; break; }
-            if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_P_FULL + (g & 1)), (g >> 1) & 1, abort_flag, p.status) &&
-                                             wait_phase(bar(Cf::B_V_FULL + v_stage), v_phase, abort_flag, p.status))) { ok = false; break; }
+            // k_stage / k_phase already name the next QK's stage (this segment
+            // or the next); at the end of the work that phase never completes
+            // and the probe just reads false
+            bool kr = k_ready;
+            const bool w = wait_pv_probe_k(bar(Cf::B_P_FULL + (g & 1)), (g >> 1) & 1, bar(Cf::B_V_FULL + v_stage),
+                                           v_phase, bar(Cf::B_K_FULL + k_stage), k_phase, kr, abort_flag, p.status);
+            k_ready = __all_sync(0xffffffffu, kr);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             tc_fence_after();
             const uint32_t p_tm = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
             const uint32_t v_base = sV + v_stage * Cf::KV_BYTES;
@@ -740,8 +789,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
                 umma_bf16_ts_warp(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
             }
             umma_commit_warp(bar(Cf::B_O_DONE + (g & 1)));
-            if (C > 1) umma_commit_multicast_warp(bar(Cf::B_V_EMPTY + v_stage), cta_mask);
-            else umma_commit_warp(bar(Cf::B_V_EMPTY + v_stage));
+            if (!soft_release) {
+              if (C > 1) umma_commit_multicast_warp(bar(Cf::B_V_EMPTY + v_stage), cta_mask);
+              else umma_commit_warp(bar(Cf::B_V_EMPTY + v_stage));
+            }
             if (++v_stage == NV) { v_stage = 0; v_phase ^= 1; }
           }
         }
@@ -824,6 +875,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         const uint32_t g = gj + jj;
         const int kv0 = kv_tile(td, sg.j0 + jj) * BN;
         if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_S_FULL + (g & 1)), (g >> 1) & 1, abort_flag, p.status))) { ok = false; break; }
+        if (soft_release && r == 0) {
+          // S(g) complete: QK(g) and every MMA issued before it, PV(g - 2)
+          // included, are done, so their K and V stages are free
+          mbar_arrive(bar(Cf::B_K_EMPTY + g % NK));
+          if (g >= 2) mbar_arrive(bar(Cf::B_V_EMPTY + (g - 2) % NV));
+        }
         tc_fence_after();
         uint32_t sr[BN];
         const uint32_t s_addr = lane_base + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
