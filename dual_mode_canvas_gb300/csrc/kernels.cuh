@@ -911,24 +911,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         }
         const float base = (m_use == -INFINITY) ? 0.f : m_use * sl2 - static_cast<float>(E::P_SHIFT);
         // p = 2^(s * scale * log2(e) - base), two lanes per fp32x2 instruction;
-        // the row sum runs in four independent fp32x2 accumulators.  With 128
-        // keys per tile the MUFU ex2 rate alone would match the MMA time, so 3
-        // of every 8 pairs take the polynomial path on the FMA pipe (measured
-        // slower for the 64-key e4m3 tiles).
-        constexpr int kPolyPairs = BN == 128 ? 3 : 0;
+        // the row sum runs in four independent fp32x2 accumulators
         const uint64_t sl2x2 = f32x2(sl2, sl2), nbase2 = f32x2(-base, -base);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[BN / E::PER_WORD];
 #pragma unroll
         for (int c = 0; c < BN; c += 2) {
-          float t0, t1, p0, p1;
+          float t0, t1;
           f32x2_split(fma_f32x2(f32x2(s[c], s[c + 1]), sl2x2, nbase2), t0, t1);
-          if (((c >> 1) & 7) < kPolyPairs) {
-            exp2_poly_x2(t0, t1, p0, p1);
-          } else {
-            p0 = ex2_approx(t0);
-            p1 = ex2_approx(t1);
-          }
+          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
           if constexpr (F8) {
             // e4m3 pairs, two per 32-bit word, lower key in the lower byte
             const uint32_t h = pack_e4m3x2(p0, p1);

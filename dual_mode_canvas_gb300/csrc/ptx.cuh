@@ -410,27 +410,6 @@ __device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// 2^x for a pair of x in [-126, 128) on the FMA pipe (no MUFU): Cody-Waite
-// range reduction x = n + f with n = round(x) (added to and subtracted from
-// 1.5 * 2^23, which leaves n in the low mantissa bits), a degree-3 minimax
-// polynomial for 2^f on [-1/2, 1/2] (coefficients from a Remez fit of the
-// relative error, max 7.5e-5), and n added to the result's exponent field.
-__device__ __forceinline__ void exp2_poly_x2(float x0, float x1, float& p0, float& p1) {
-  const uint64_t magic = f32x2(12582912.f, 12582912.f);
-  const uint64_t x = f32x2(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-  const uint64_t t = add_f32x2(x, magic);
-  const uint64_t f = sub_f32x2(x, sub_f32x2(t, magic));
-  uint64_t q = fma_f32x2(f, f32x2(0.05517166905792616f, 0.05517166905792616f),
-                         f32x2(0.2426111221932161f, 0.2426111221932161f));
-  q = fma_f32x2(q, f, f32x2(0.6932609854606553f, 0.6932609854606553f));
-  q = fma_f32x2(q, f, f32x2(0.9999280735394012f, 0.9999280735394012f));
-  float q0, q1, t0, t1;
-  f32x2_split(q, q0, q1);
-  f32x2_split(t, t0, t1);
-  p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
-  p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
-}
-
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
