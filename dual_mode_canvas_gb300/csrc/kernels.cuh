@@ -523,10 +523,14 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
   // barriers
-  static constexpr int B_Q_FULL = 0, B_K_FULL = 1, B_K_EMPTY = 1 + NK,
-                       B_V_FULL = 1 + 2 * NK, B_V_EMPTY = 1 + 2 * NK + NV,
-                       B_S_FULL = 1 + 2 * NK + 2 * NV, B_P_FULL = B_S_FULL + 2,
-                       B_O_DONE = B_P_FULL + 2, B_O_FREE = B_O_DONE + 2,
+  // S_FULL[s]: QK^T of the tile in K stage s is done in every CTA of the
+  // cluster (which also frees that K stage); O_DONE[s]: likewise P.V of the
+  // tile in V stage s (which frees that V stage)
+  // (with soft release, K_EMPTY / V_EMPTY free the stages instead)
+  static constexpr int B_Q_FULL = 0, B_K_FULL = 1, B_V_FULL = 1 + NK,
+                       B_S_FULL = 1 + NK + NV, B_P_FULL = B_S_FULL + NK,
+                       B_O_DONE = B_P_FULL + 2, B_K_EMPTY = B_O_DONE + NV, B_V_EMPTY = B_K_EMPTY + NK,
+                       B_O_FREE = B_V_EMPTY + NV,
                        B_DRAIN = B_O_FREE + 1, NUM_BARS = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
@@ -573,8 +577,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   const int64_t u_beg = cta_unit_begin(cl, U, P);
   const int64_t u_end = cta_unit_begin(cl + 1, U, P);
   const uint16_t cta_mask = static_cast<uint16_t>((1u << C) - 1u);
-  // K / V stages released by a softmax thread (see the MMA issuer) or by
-  // tcgen05.commit from the MMA warp
+  // Soft release (64-key tiles, no cluster): a softmax thread frees the K and
+  // V stages with an arrive once it has seen S(g), so the loaders wait on
+  // K_EMPTY / V_EMPTY; measured 1.5% faster there than freeing them through
+  // the MMA warp's S_FULL / O_DONE commits, which the other shapes use.
   const bool soft_release = (BN == 64) && (C == 1);
 
   const uint32_t sK = sbase + Cf::OFF_K;
@@ -586,26 +592,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Cf::B_Q_FULL), kRows);
-    // a K/V slot is free once every CTA of the cluster has consumed it: C
-    // commits from the MMA warps, or (soft_release, C == 1) one softmax arrive
+    // S_FULL / O_DONE count one commit from the MMA warp of every CTA of the
+    // cluster (multicast).  Tile g uses S_FULL[g % NK] and O_DONE[g % NV]: a
+    // wait for tile x never aliases, since the next tile on the same barrier,
+    // x + NK (x + NV), cannot be issued before P(x) exists.
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(Cf::B_K_FULL + s), 1);
-      mbar_init(bar(Cf::B_K_EMPTY + s), C);
+      mbar_init(bar(Cf::B_S_FULL + s), C);
+      mbar_init(bar(Cf::B_K_EMPTY + s), 1);
     }
     for (int s = 0; s < NV; ++s) {
       mbar_init(bar(Cf::B_V_FULL + s), 1);
-      mbar_init(bar(Cf::B_V_EMPTY + s), C);
+      mbar_init(bar(Cf::B_O_DONE + s), C);
+      mbar_init(bar(Cf::B_V_EMPTY + s), 1);
     }
-    // one S_FULL / P_FULL / O_DONE per S/P buffer: tile g uses index g & 1
-    mbar_init(bar(Cf::B_S_FULL + 0), 1);
-    mbar_init(bar(Cf::B_S_FULL + 1), 1);
+    // one P_FULL per S/P buffer in TMEM: tile g uses index g & 1
     mbar_init(bar(Cf::B_P_FULL + 0), kRows);
     mbar_init(bar(Cf::B_P_FULL + 1), kRows);
-    // PV(g) arrives on O_DONE[g & 1].  A wait for PV(x) then never aliases:
-    // S(x) (already seen) implies PV(x - 2) is done, and PV(x + 2) cannot run
-    // before P(x + 2) exists.
-    mbar_init(bar(Cf::B_O_DONE + 0), 1);
-    mbar_init(bar(Cf::B_O_DONE + 1), 1);
     mbar_init(bar(Cf::B_O_FREE), kRows);
     mbar_init(bar(Cf::B_DRAIN), 1);
     *abort_flag = 0;
@@ -639,7 +642,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       const int slice = BN / C;                                               // rows per CTA
       const int NS = is_k ? NK : NV;
       const uint32_t full0 = bar(is_k ? Cf::B_K_FULL : Cf::B_V_FULL);
-      const uint32_t empty0 = bar(is_k ? Cf::B_K_EMPTY : Cf::B_V_EMPTY);
+      // a stage is free once its tile's QK^T (K) or P.V (V) is done in every CTA
+      const uint32_t empty0 = soft_release ? bar(is_k ? Cf::B_K_EMPTY : Cf::B_V_EMPTY)
+                                           : bar(is_k ? Cf::B_S_FULL : Cf::B_O_DONE);
       const uint32_t ring = is_k ? sK : sV;
       const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
       uint32_t stage = 0, phase = 0;
@@ -725,10 +730,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     //
     // This warp's loop sets the pace: every mbarrier test and every commit
     // costs it 100-300 clocks, against ~1000 clocks of MMAs per tile.  So it
-    // tests P, V and the next K together, and, where the softmax warps have
-    // time to spare (64-key tiles, no cluster), leaves the release of the K
-    // and V stages to them (soft_release) instead of committing to the empty
-    // barriers itself.
+    // tests P, V and the next K together, and commits once per MMA batch: the
+    // commit that tells the softmax warps S is ready also frees the K stage,
+    // the one that marks P.V done also frees the V stage (or, with soft
+    // release, a softmax thread frees both).
     {
       constexpr uint32_t idesc_qk = F8 ? idesc_e4m3_f32(kRows, BN, 0, 0) : idesc_bf16_f32(kRows, BN, 0, 0);
       constexpr uint32_t idesc_pv = F8 ? idesc_e4m3_f32(kRows, D, 0, 1) : idesc_bf16_f32(kRows, D, 0, 1);
@@ -757,11 +762,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
               if constexpr (F8) umma_e4m3_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
               else umma_bf16_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            umma_commit_warp(bar(Cf::B_S_FULL + (g & 1)));
-            if (!soft_release) {
-              if (C > 1) umma_commit_multicast_warp(bar(Cf::B_K_EMPTY + k_stage), cta_mask);
-              else umma_commit_warp(bar(Cf::B_K_EMPTY + k_stage));
-            }
+            if (C > 1) umma_commit_multicast_warp(bar(Cf::B_S_FULL + k_stage), cta_mask);
+            else umma_commit_warp(bar(Cf::B_S_FULL + k_stage));
             if (++k_stage == NK) { k_stage = 0; k_phase ^= 1; }
           }
           if (jj >= 1) {
@@ -788,11 +790,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
               else
                 umma_bf16_ts_warp(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
             }
-            umma_commit_warp(bar(Cf::B_O_DONE + (g & 1)));
-            if (!soft_release) {
-              if (C > 1) umma_commit_multicast_warp(bar(Cf::B_V_EMPTY + v_stage), cta_mask);
-              else umma_commit_warp(bar(Cf::B_V_EMPTY + v_stage));
-            }
+            if (C > 1) umma_commit_multicast_warp(bar(Cf::B_O_DONE + v_stage), cta_mask);
+            else umma_commit_warp(bar(Cf::B_O_DONE + v_stage));
             if (++v_stage == NV) { v_stage = 0; v_phase ^= 1; }
           }
         }
@@ -874,7 +873,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       for (int jj = 0; jj < n; ++jj) {
         const uint32_t g = gj + jj;
         const int kv0 = kv_tile(td, sg.j0 + jj) * BN;
-        if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_S_FULL + (g & 1)), (g >> 1) & 1, abort_flag, p.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_S_FULL + g % NK), (g / NK) & 1, abort_flag, p.status))) { ok = false; break; }
         if (soft_release && r == 0) {
           // S(g) complete: QK(g) and every MMA issued before it, PV(g - 2)
           // included, are done, so their K and V stages are free
@@ -941,7 +940,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         if (jj > 0 && __any_sync(0xffffffffu, rescale)) {
           // the row maximum grew by more than 2^8: rescale O once PV(g-1) is done
           const uint32_t x = g - 1;
-          if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_O_DONE + (x & 1)), (x >> 1) & 1, abort_flag, p.status))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_O_DONE + x % NV), (x / NV) & 1, abort_flag, p.status))) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -962,7 +961,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       // PV(g_last) done implies every earlier MMA of this CTA is done
       {
         const uint32_t x = gj + n - 1;
-        if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_O_DONE + (x & 1)), (x >> 1) & 1, abort_flag, p.status))) {
+        if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_O_DONE + x % NV), (x / NV) & 1, abort_flag, p.status))) {
           ok = false;
           break;
         }
