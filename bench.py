@@ -46,7 +46,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum of one main-kernel launch, from the ncu
 # capture summarised in profiles/ (kept only while the kernel is unchanged since that capture)
-NCU_TRAFFIC_BYTES = {"denoise_loop": 1.802e8, "denoise_loop:e4m3": 7.624e7, "maxmix_full": 2.929e9}
+NCU_TRAFFIC_BYTES = {"denoise_loop": 1.794e8, "denoise_loop:e4m3": 7.585e7, "maxmix_full": 2.927e9}
 
 
 def visible_pairs(wl) -> int:
