@@ -1061,13 +1061,68 @@ combine_kernel(const FwdParams p, int num_clusters) {
   };
   // the partials are written by the attention grid, this grid's predecessor
   griddep_wait();
+  constexpr int E = D / 32;  // columns per lane
+  const int orow = td.q_row0 + t;
+  const int h = td.kvh * G + gi;
+  __nv_bfloat16* dst = p.out + (static_cast<size_t>(orow) * p.Hq + h) * D;
+  if (nc <= 4) {
+    // the usual case: every load of the row (up to four contributors' LSE and
+    // columns) is issued at once, one memory round trip in all
+    float lw[4];
+    float acc4[4][E];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int sl = slot_of(c_lo + min(u, nc - 1));
+      lw[u] = u < nc ? p.ws.part_lse[static_cast<size_t>(sl) * kRows + r] : -INFINITY;
+      const float* src = p.ws.part_o + (static_cast<size_t>(sl) * kRows + r) * D;
+      if constexpr (E % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < E / 4; ++k) {
+          const float4 x = u < nc ? *reinterpret_cast<const float4*>(src + (k * 32 + lane) * 4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          acc4[u][4 * k + 0] = x.x;
+          acc4[u][4 * k + 1] = x.y;
+          acc4[u][4 * k + 2] = x.z;
+          acc4[u][4 * k + 3] = x.w;
+        }
+      } else {
+        const float2 x = u < nc ? *reinterpret_cast<const float2*>(src + lane * 2) : make_float2(0.f, 0.f);
+        acc4[u][0] = x.x;
+        acc4[u][1] = x.y;
+      }
+    }
+    const float M4 = fmaxf(fmaxf(lw[0], lw[1]), fmaxf(lw[2], lw[3]));
+    float wsum4 = 0.f, acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = lw[u] == -INFINITY ? 0.f : __expf(lw[u] - M4);
+      wsum4 += w;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += w * acc4[u][e];
+    }
+    const float inv4 = wsum4 > 0.f ? 1.f / wsum4 : 0.f;
+    if constexpr (E % 4 == 0) {
+#pragma unroll
+      for (int k = 0; k < E / 4; ++k) {
+        const uint32_t w0 = pack_bf16x2(acc[4 * k + 0] * inv4, acc[4 * k + 1] * inv4);
+        const uint32_t w1 = pack_bf16x2(acc[4 * k + 2] * inv4, acc[4 * k + 3] * inv4);
+        *reinterpret_cast<uint2*>(dst + (k * 32 + lane) * 4) = make_uint2(w0, w1);
+      }
+    } else {
+      *reinterpret_cast<uint32_t*>(dst + lane * 2) = pack_bf16x2(acc[0] * inv4, acc[1] * inv4);
+    }
+    if (lane == 0 && p.lse != nullptr)
+      p.lse[static_cast<size_t>(orow) * p.Hq + h] = wsum4 > 0.f ? M4 + logf(wsum4) : -INFINITY;
+    return;
+  }
   // every contributor's LSE at once (lane i holds contributors i, i + 32, ...)
   float M = -INFINITY;
   for (int i = lane; i < nc; i += 32)
     M = fmaxf(M, p.ws.part_lse[static_cast<size_t>(slot_of(c_lo + i)) * kRows + r]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  constexpr int E = D / 32;  // columns per lane
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
@@ -1122,9 +1177,6 @@ combine_kernel(const FwdParams p, int num_clusters) {
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const int orow = td.q_row0 + t;
-  const int h = td.kvh * G + gi;
-  __nv_bfloat16* dst = p.out + (static_cast<size_t>(orow) * p.Hq + h) * D;
   if constexpr (E % 4 == 0) {
 #pragma unroll
     for (int k = 0; k < E / 4; ++k) {
