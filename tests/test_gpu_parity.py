@@ -199,12 +199,14 @@ def test_split_kv_matches_single_cta():
     assert ((lse_split - lse_one).abs() <= lse_order_bound(lse_split, lse_one, 3256)).all()
 
 
+@pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("ctas", ["152", "10"])
-def test_rotated_kv_order_matches_ascending(ctas):
+def test_rotated_kv_order_matches_ascending(ctas, D):
     """Visiting each group's KV tiles from a rotated start (the default) gives
     the ascending-order result up to fp32 rounding, with the cut points of the
-    full grid and of a 10-CTA grid (many cuts inside each group)."""
-    wl, batch = wls.random_batch(10, ((3000, 256, 1), (1000, 300, 0), (500, 64, 1)), 8, 2, 128, -1)
+    full grid and of a 10-CTA grid (many cuts inside each group); head_dim 256
+    runs unclustered with the softmax-side stage release, 128 in pairs."""
+    wl, batch = wls.random_batch(10 + D, ((3000, 256, 1), (1000, 300, 0), (500, 64, 1)), 8, 2, D, -1)
     dev = to_dev(batch)
     os.environ["DG_ATTN_NUM_CTAS"] = ctas
     try:
@@ -216,7 +218,7 @@ def test_rotated_kv_order_matches_ascending(ctas):
             finally:
                 del os.environ["DG_ATTN_KV_ORDER"]
             assert (out_rot.float() - out_lin.float()).abs().max().item() <= 2 ** -7, W
-            assert ((lse_rot - lse_lin).abs() <= lse_order_bound(lse_rot, lse_lin, 3256)).all(), W
+            assert ((lse_rot - lse_lin).abs() <= lse_order_bound(lse_rot, lse_lin, 3256, 128 if D == 128 else 64)).all(), W
     finally:
         del os.environ["DG_ATTN_NUM_CTAS"]
 
