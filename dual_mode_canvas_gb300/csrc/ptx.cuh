@@ -164,34 +164,13 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, issued by
-// one thread.  accumulate == 0 overwrites D.
-__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T: A is M rows (one per TMEM lane) x K
-// bf16 elements packed two per 32-bit column (the lower half holds the even
-// element); a K=16 step spans 8 columns.
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Warp-wide forms: every lane of the warp executes them with identical
-// operands; elect.sync picks one lane (the lowest, the same one every time
-// while the warp is converged) that actually issues.
+// tcgen05 MMAs and commits in warp-wide form: every lane of the warp executes
+// them with identical operands; elect.sync picks one lane (the lowest, the
+// same one every time while the warp is converged) that actually issues.
+//
+// D[tmem] (+)= A[tmem] * B[smem]^T: A is M rows (one per TMEM lane) x K bf16
+// elements packed two per 32-bit column (the lower half holds the even
+// element); a K=16 step spans 8 columns.  accumulate == 0 overwrites D.
 __device__ __forceinline__ void umma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                   uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -213,6 +192,8 @@ __device__ __forceinline__ void umma_e4m3_ts_warp(uint32_t d_tmem, uint32_t a_tm
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Arrive (once) on `bar` when every tcgen05 op issued so far by this thread
+// has completed.
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -220,28 +201,13 @@ __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
+// Same, arriving on the mbarrier at this offset in every CTA named in cta_mask.
 __device__ __forceinline__ void umma_commit_multicast_warp(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;\n\t}" ::"r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
-// Arrive (once) on `bar` when every tcgen05 op issued so far by this thread
-// has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-
-// Same, arriving on the mbarrier at this offset in every CTA named in cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
       : "memory");
 }
 
