@@ -8,6 +8,7 @@ raise.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -26,6 +27,9 @@ DG_ERR_DEVICE_BOUNDS = 6
 DG_MODE_CAUSAL = 0
 DG_MODE_BIDIRECTIONAL = 1
 
+# capacity of dg_attn_forward_noalloc's static scratch (DG_ATTN_NOALLOC_SCRATCH_BYTES)
+NOALLOC_SCRATCH_BYTES = 48 << 20
+
 EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profiled",
             "dg_attn_forward_noalloc", "dg_attn_forward_paged", "dg_attn_forward_paged_profiled",
             "dg_attn_forward_fp8", "dg_attn_forward_fp8_profiled",
@@ -34,7 +38,8 @@ EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profil
             "dg_sampler_step",
             "dg_attn_status", "dg_attn_error_string", "dg_attn_version")
 
-_lib = None
+_libs = {}        # loaded libraries: False -> the library, True -> the checking build
+_use_debug = False
 
 
 class DgAttnError(RuntimeError):
@@ -43,16 +48,19 @@ class DgAttnError(RuntimeError):
         super().__init__(f"{where}: {error_string(code)} (status {code})")
 
 
-def library_path() -> str:
-    return _build.LIB
+def library_path(debug: bool = False) -> str:
+    return _build.lib_path(debug)
 
 
-def load_library():
-    """Loads ``lib/libdg_attn.so`` (built by ``build.build()``); raises if absent."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    path = library_path()
+def load_library(debug: bool | None = None):
+    """Loads ``lib/libdg_attn.so`` (built by ``build.build_all()``); raises if
+    absent.  ``debug=True`` loads the bounds-checking build
+    ``lib/libdg_attn_debug.so`` instead; by default the one selected by
+    ``debug_library()`` (the library itself outside it)."""
+    dbg = _use_debug if debug is None else bool(debug)
+    if dbg in _libs:
+        return _libs[dbg]
+    path = library_path(dbg)
     if not os.path.exists(path):
         raise RuntimeError(f"dg_attn CUDA library not built ({path}); run __graft_entry__.build()")
     lib = ctypes.CDLL(path)
@@ -102,8 +110,21 @@ def load_library():
     lib.dg_attn_error_string.restype = ctypes.c_char_p
     lib.dg_attn_version.argtypes = []
     lib.dg_attn_version.restype = i32
-    _lib = lib
+    _libs[dbg] = lib
     return lib
+
+
+@contextlib.contextmanager
+def debug_library():
+    """Within the block every call of this module goes to the bounds-checking
+    build (its own status word included)."""
+    global _use_debug
+    prev = _use_debug
+    _use_debug = True
+    try:
+        yield load_library()
+    finally:
+        _use_debug = prev
 
 
 def error_string(code: int) -> str:

@@ -32,16 +32,9 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kVersion = 100;  // 0.1.0
 
-constexpr int kClusterSizes[] = {1, 2, 4, 8};
-
-int cluster_slot(int C) { return C == 1 ? 0 : C == 2 ? 1 : C == 4 ? 2 : 3; }
-int dim_slot(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
-
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
-  int max_clusters[2][3][4] = {};  // [e4m3][head_dim][cluster size]: co-resident clusters
-  int sc_max_clusters[2] = {};  // self-conditioning kernel, clusters of 1 / 2
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;   // device address of g_status
   void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
@@ -77,57 +70,15 @@ int kv_tile_rows(int D, bool f8 = false) {
 }
 
 template <int D, bool F8 = false>
-cudaError_t set_kernel_attrs(DeviceInfo& di) {
+cudaError_t set_kernel_attrs() {
   using S = Shape<D, F8>;
   using C = FwdCfg<D, S::BN, S::NK, S::NV, F8>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV, F8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  // how many clusters of each size fit on the device at once (persistent grid)
-  for (int cs : kClusterSizes) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs * (di.num_sms / cs));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel<D, S::BN, S::NK, S::NV, F8>, &cfg) != cudaSuccess)
-      n = 0;
-    di.max_clusters[F8 ? 1 : 0][dim_slot(D)][cluster_slot(cs)] = n;
-  }
-  cudaGetLastError();
-  return cudaSuccess;
+  return cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV, F8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
 }
 
-cudaError_t set_sc_attrs(DeviceInfo& di) {
-  cudaError_t e = cudaFuncSetAttribute(sc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       ScCfg::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  for (int i = 0; i < 2; ++i) {
-    const int cs = i + 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs * (di.num_sms / cs));
-    cfg.blockDim = dim3(kScThreads);
-    cfg.dynamicSmemBytes = ScCfg::SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sc_kernel, &cfg) != cudaSuccess) n = 0;
-    di.sc_max_clusters[i] = n;
-  }
-  cudaGetLastError();
-  return cudaSuccess;
+cudaError_t set_sc_attrs() {
+  return cudaFuncSetAttribute(sc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ScCfg::SMEM_BYTES);
 }
 
 // One-time per-device setup (SM count, architecture, kernel attributes,
@@ -154,9 +105,9 @@ dg_status_t device_info(DeviceInfo** out) {
         return DG_ERR_CUDA;
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    if (set_kernel_attrs<64>(di) != cudaSuccess || set_kernel_attrs<128>(di) != cudaSuccess ||
-        set_kernel_attrs<256>(di) != cudaSuccess || set_kernel_attrs<128, true>(di) != cudaSuccess ||
-        set_kernel_attrs<256, true>(di) != cudaSuccess || set_sc_attrs(di) != cudaSuccess)
+    if (set_kernel_attrs<64>() != cudaSuccess || set_kernel_attrs<128>() != cudaSuccess ||
+        set_kernel_attrs<256>() != cudaSuccess || set_kernel_attrs<128, true>() != cudaSuccess ||
+        set_kernel_attrs<256, true>() != cudaSuccess || set_sc_attrs() != cudaSuccess)
       return DG_ERR_CUDA;
     void* sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status) != cudaSuccess) return DG_ERR_CUDA;
@@ -172,44 +123,19 @@ dg_status_t device_info(DeviceInfo** out) {
   return DG_OK;
 }
 
-// Cluster size for a call: C query tiles of one (sequence, KV head) share
-// every K/V load.  DG_ATTN_CLUSTER (1, 2, 4 or 8) overrides the default.
-// A paged cache with pages smaller than half a KV tile is loaded one page per
-// TMA box: a larger cluster gives each CTA a shorter slice, so fewer boxes,
-// and shares each of them more widely (measured on 16-row pages and 128-key
-// tiles: clusters of 4 take 1.02 ms where clusters of 2 take 1.14 ms and the
-// contiguous layout 0.98 ms).  Contiguous K/V with the rotated KV order (most
-// reads are L2 hits, so multicast saves little): head_dim 128 runs best in
-// pairs (max mix 1.019 vs 1.028 ms per step unpaired), head_dim 256 unpaired
-// (denoise step 0.242 vs 0.247 ms in pairs; e4m3 0.196 vs 0.205 ms).
-int cluster_for(const DeviceInfo& di, int D, bool f8 = false, int page_size = 0) {
-  int C = D == 256 ? 1 : 2;
-  if (page_size > 0) {
-    const int BN = kv_tile_rows(D, f8);
-    if (page_size * 2 < BN) C = std::min(4, std::max(2, BN / (2 * page_size)));
-  }
-  if (const char* e = std::getenv("DG_ATTN_CLUSTER")) {
-    const int v = std::atoi(e);
-    if (v == 1 || v == 2 || v == 4 || v == 8) C = v;
-  }
-  while (C > 1 && di.max_clusters[f8 ? 1 : 0][dim_slot(D)][cluster_slot(C)] < 1) C >>= 1;
-  return C;
-}
-
-// Each group's KV tiles are visited in the rotated order that lines up the
-// clusters streaming the same KV (DG_ATTN_KV_ORDER=linear: ascending order).
+// Each query tile's KV tiles are visited in the rotated order that lines up
+// the CTAs streaming the same KV (DG_ATTN_KV_ORDER=linear: ascending order).
 bool rotate_kv_order() {
   const char* e = std::getenv("DG_ATTN_KV_ORDER");
   return !(e && std::strcmp(e, "linear") == 0);
 }
 
-// Persistent grid: as many clusters as are co-resident (DG_ATTN_NUM_CTAS caps
-// the number of CTAs, for tests of the split-KV path).
-int num_clusters_for(const DeviceInfo& di, int D, int C, bool f8 = false) {
-  int n = C == 1 ? di.num_sms : di.max_clusters[f8 ? 1 : 0][dim_slot(D)][cluster_slot(C)];
-  if (n < 1) n = 1;
+// Persistent grid: one CTA per SM (DG_ATTN_NUM_CTAS caps the number of CTAs,
+// for tests of the split-KV path).
+int num_ctas_for(const DeviceInfo& di) {
+  int n = di.num_sms;
   if (const char* e = std::getenv("DG_ATTN_NUM_CTAS")) {
-    const int v = std::max(1, std::atoi(e) / C);
+    const int v = std::max(1, std::atoi(e));
     if (v < n) n = v;
   }
   return n;
@@ -232,7 +158,7 @@ Layout make_layout(int B, int total_q, int Hq, int Hkv, int D, int num_sms) {
   l.hdr = off;        off = align256(off + sizeof(WorkHeader));
   l.seq_tile = off;   off = align256(off + sizeof(int64_t) * (B + 1));
   l.seq_kv = off;     off = align256(off + sizeof(int64_t) * (B + 1));
-  l.tiles = off;      off = align256(off + sizeof(TileDesc) * kMaxCluster * static_cast<size_t>(l.max_tiles));
+  l.tiles = off;      off = align256(off + sizeof(TileDesc) * static_cast<size_t>(l.max_tiles));
   l.unit_begin = off; off = align256(off + sizeof(int64_t) * (static_cast<size_t>(l.max_tiles) + 1));
   l.part_lse = off;   off = align256(off + sizeof(float) * 2 * static_cast<size_t>(num_sms) * kRows);
   l.part_o = off;     off = align256(off + sizeof(float) * 2 * static_cast<size_t>(num_sms) * kRows * D);
@@ -269,33 +195,29 @@ dg_status_t encode_map(CUtensorMap* map, const void* base, int rows, int heads, 
 
 template <int D, bool F8 = false>
 dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
-                   const FwdParams& p, int num_clusters, int max_groups, cudaStream_t stream,
+                   const FwdParams& p, int num_ctas, int max_tiles, cudaStream_t stream,
                    cudaEvent_t ev_begin, cudaEvent_t ev_end) {
   using S = Shape<D, F8>;
   using C = FwdCfg<D, S::BN, S::NK, S::NV, F8>;
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DG_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_clusters * p.C);
+  cfg.gridDim = dim3(num_ctas);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[1];
   // programmatic dependent of the work-list grid (the kernel waits for it)
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV, F8>, mk, mv, p) != cudaSuccess)
     return DG_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return DG_ERR_CUDA;
   // the merge is a programmatic dependent of the attention grid (it waits
   // for it before reading the partials)
   cudaLaunchConfig_t ccfg = {};
-  ccfg.gridDim = dim3(max_groups * p.C, (kRows + kCombineWarps - 1) / kCombineWarps);
+  ccfg.gridDim = dim3(max_tiles, (kRows + kCombineWarps - 1) / kCombineWarps);
   ccfg.blockDim = dim3(kCombineWarps * 32);
   ccfg.stream = stream;
   cudaLaunchAttribute cattr[1];
@@ -303,7 +225,7 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
   cattr[0].val.programmaticStreamSerializationAllowed = 1;
   ccfg.attrs = cattr;
   ccfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&ccfg, combine_kernel<D>, p, num_clusters) != cudaSuccess) return DG_ERR_CUDA;
+  if (cudaLaunchKernelEx(&ccfg, combine_kernel<D>, p, num_ctas) != cudaSuccess) return DG_ERR_CUDA;
   return DG_OK;
 }
 
@@ -324,6 +246,36 @@ extern "C" size_t dg_attn_workspace_size(int32_t num_seqs, int32_t total_q, int3
 }
 
 namespace {
+// The host-visible argument checks of a forward call (everything but the
+// workspace).  *nothing_to_do is set when the call is valid and has no work
+// (no sequences or no query tokens).
+dg_status_t check_args(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                       const int32_t* ctx_len, const uint8_t* mode, int32_t num_seqs,
+                       int32_t total_q, int32_t total_kv, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t window, float scale, const void* out,
+                       const float* lse, bool paged, bool f8, bool* nothing_to_do) {
+  *nothing_to_do = false;
+  if (f8 && (head_dim == 64 || paged)) return DG_ERR_UNSUPPORTED;
+  if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim))
+    return (num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
+            num_q_heads / num_kv_heads > kRows) || (head_dim > 0 && head_dim != 64 &&
+            head_dim != 128 && head_dim != 256 && head_dim % 8 == 0)
+               ? DG_ERR_UNSUPPORTED
+               : DG_ERR_INVALID_ARG;
+  if (window < -1 || total_kv < 0 || !(scale > 0.f) || !std::isfinite(scale)) return DG_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) {
+    *nothing_to_do = true;
+    return num_seqs == 0 && total_q != 0 ? DG_ERR_INVALID_ARG : DG_OK;
+  }
+  if (!paged && total_kv < total_q) return DG_ERR_INVALID_ARG;
+  if (!paged && (!k || !v || !aligned(k, 16) || !aligned(v, 16))) return DG_ERR_INVALID_ARG;
+  if (!q || !cu_q || !ctx_len || !mode || !out) return DG_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) ||
+      !aligned(cu_q, 4) || !aligned(ctx_len, 4) || (lse && !aligned(lse, 4)))
+    return DG_ERR_INVALID_ARG;
+  return DG_OK;
+}
+
 // `pg` null: contiguous K/V (k, v, total_kv); otherwise the paged cache it
 // describes (k, v unused).
 dg_status_t forward_impl(const void* q, const void* k, const void* v, const int32_t* cu_q,
@@ -335,22 +287,11 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
                          const PagedArgs* pg = nullptr, const float* e4m3_scales = nullptr) {
   // e4m3_scales = {q, k, v} scales: Q, K, V are e4m3 bytes (contiguous layout only)
   const bool f8 = e4m3_scales != nullptr;
-  if (f8 && (head_dim == 64 || pg)) return DG_ERR_UNSUPPORTED;
-  if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim))
-    return (num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
-            num_q_heads / num_kv_heads > kRows) || (head_dim > 0 && head_dim != 64 &&
-            head_dim != 128 && head_dim != 256 && head_dim % 8 == 0)
-               ? DG_ERR_UNSUPPORTED
-               : DG_ERR_INVALID_ARG;
-  if (window < -1 || total_kv < 0 || !(scale > 0.f) || !std::isfinite(scale)) return DG_ERR_INVALID_ARG;
-  if (num_seqs == 0) return total_q == 0 ? DG_OK : DG_ERR_INVALID_ARG;
-  if (total_q == 0) return DG_OK;
-  if (!pg && total_kv < total_q) return DG_ERR_INVALID_ARG;
-  if (!pg && (!k || !v || !aligned(k, 16) || !aligned(v, 16))) return DG_ERR_INVALID_ARG;
-  if (!q || !cu_q || !ctx_len || !mode || !out) return DG_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(out, 16) ||
-      !aligned(cu_q, 4) || !aligned(ctx_len, 4) || (lse && !aligned(lse, 4)))
-    return DG_ERR_INVALID_ARG;
+  bool nothing_to_do = false;
+  const dg_status_t chk = check_args(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv,
+                                     num_q_heads, num_kv_heads, head_dim, window, scale, out, lse,
+                                     pg != nullptr, f8, &nothing_to_do);
+  if (chk != DG_OK || nothing_to_do) return chk;
 
   DeviceInfo* di = nullptr;
   const dg_status_t st = device_info(&di);
@@ -361,12 +302,9 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   const int G = num_q_heads / num_kv_heads;
   const int TT = kRows / G;
   const int BN = kv_tile_rows(head_dim, f8);
-  const int Ccl = cluster_for(*di, head_dim, f8, pg ? (1 << pg->page_shift) : 0);
   CUtensorMap mk, mv;
-  // each CTA of a cluster loads BN / C rows of every K/V tile; from a paged
-  // cache in boxes of at most one page
-  const int slice = BN / Ccl;
-  const int box = pg ? std::min(1 << pg->page_shift, slice) : slice;
+  // K/V tiles of BN rows; from a paged cache in boxes of at most one page
+  const int box = pg ? std::min(1 << pg->page_shift, BN) : BN;
   const void* kmap = pg ? pg->k_cache : k;
   const void* vmap = pg ? pg->v_cache : v;
   const int map_rows = pg ? (pg->num_pages << pg->page_shift) : total_kv;
@@ -391,12 +329,19 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.G = G;
   p.TT = TT;
   p.window = window;
-  p.C = Ccl;
   p.block_table = pg ? pg->block_table : nullptr;
   p.page_shift = pg ? pg->page_shift : 0;
   p.page_box = box;
   p.debug_skip_k_load = -1;
   if (const char* e = std::getenv("DG_ATTN_DEBUG_SKIP_K_LOAD")) p.debug_skip_k_load = std::atoi(e);
+  p.Hkv = num_kv_heads;
+  p.kv_rows = map_rows;
+  p.total_q = total_q;
+  p.bt_entries = pg ? static_cast<int64_t>(num_seqs) * pg->bt_stride : 0;
+  p.debug_bad_kv_row = -1;
+#ifdef DG_ATTN_DEBUG
+  if (const char* e = std::getenv("DG_ATTN_DEBUG_BAD_KV_ROW")) p.debug_bad_kv_row = std::atoi(e);
+#endif
   // e4m3: the q and k scales multiply every score, the v scale the output
   const float s_eff = f8 ? scale * e4m3_scales[0] * e4m3_scales[1] : scale;
   p.scale = s_eff;
@@ -413,20 +358,21 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
       append_ctas = static_cast<int>(std::min<int64_t>((units + 1023) / 1024, 2ll * di->num_sms));
     }
   }
-  const int num_clusters = num_clusters_for(*di, head_dim, Ccl, f8);
+  const int num_ctas = num_ctas_for(*di);
+  p.num_slots = 2 * num_ctas;
   build_worklist_kernel<<<1 + append_ctas, 1024, 0, stream>>>(
       cu_q, ctx_len, mode, num_seqs, total_q, pg ? INT32_MAX : total_kv, num_kv_heads, TT, BN,
-      window, lay.max_tiles, Ccl, num_clusters, rotate_kv_order() ? 1 : 0, p.ws, pa, p.status);
+      window, lay.max_tiles, num_ctas, rotate_kv_order() ? 1 : 0, p.ws, pa, p.status);
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
   if (f8) {
-    if (head_dim == 128) return launch<128, true>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
-    return launch<256, true>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
+    if (head_dim == 128) return launch<128, true>(mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
+    return launch<256, true>(mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
   }
   switch (head_dim) {
-    case 64: return launch<64>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
-    case 128: return launch<128>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
-    default: return launch<256>(mk, mv, p, num_clusters, lay.max_tiles, stream, e0, e1);
+    case 64: return launch<64>(mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
+    case 128: return launch<128>(mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
+    default: return launch<256>(mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);
   }
 }
 }  // namespace
@@ -466,11 +412,13 @@ extern "C" dg_status_t dg_attn_forward_noalloc(const void* q, const void* k, con
                                                int32_t head_dim, int32_t window, float scale,
                                                void* out, float* lse, void* stream) {
   NvtxRange nvtx("dg_attn_forward_noalloc");
-  if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim) || num_seqs == 0 ||
-      total_q == 0)
-    return forward_impl(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv, num_q_heads,
-                        num_kv_heads, head_dim, window, scale, out, lse, nullptr, 0, stream,
-                        nullptr, nullptr);
+  // the same argument checks as dg_attn_forward first, so a bad argument
+  // reports DG_ERR_INVALID_ARG / DG_ERR_UNSUPPORTED whatever the sizes
+  bool nothing_to_do = false;
+  const dg_status_t chk = check_args(q, k, v, cu_q, ctx_len, mode, num_seqs, total_q, total_kv,
+                                     num_q_heads, num_kv_heads, head_dim, window, scale, out, lse,
+                                     false, false, &nothing_to_do);
+  if (chk != DG_OK || nothing_to_do) return chk;
   DeviceInfo* di = nullptr;
   const dg_status_t st = device_info(&di);
   if (st != DG_OK) return st;
@@ -602,32 +550,30 @@ int stat_chunks(int32_t vocab) {
 namespace {
 int stat_chunks(int32_t vocab);
 
-// Self-conditioning plan: tiles, cluster size, vocabulary splits and the
-// workspace layout.  The split count depends only on the shapes and the SM
-// count, so the size query and the call agree.
+// Self-conditioning plan: tiles, vocabulary splits and the workspace layout.
+// The split count depends only on the shapes and the SM count, so the size
+// query and the call agree.
 struct ScPlan {
-  int C, m_tiles, n_tiles, m_groups, splits, kblocks, chunks;
+  int m_tiles, n_tiles, splits, kblocks, chunks;
   size_t off_stats, off_rowc, off_part, total;
 };
 
 ScPlan sc_plan(int rows, int vocab, int d, int num_sms) {
   ScPlan pl;
   pl.m_tiles = (rows + kRows - 1) / kRows;
-  pl.C = pl.m_tiles >= 2 ? 2 : 1;
-  pl.m_groups = (pl.m_tiles + pl.C - 1) / pl.C;
   pl.n_tiles = (d + kScN - 1) / kScN;
   pl.kblocks = (vocab + kScK - 1) / kScK;
   pl.chunks = stat_chunks(vocab);
-  // split the vocabulary so the units spread evenly over the clusters:
-  // minimise ceil(units / clusters) / splits (the time of the busiest
-  // cluster), keeping at least 8 blocks per split
-  const int64_t per_split = static_cast<int64_t>(pl.m_groups) * pl.n_tiles;
-  const int clusters = std::max(1, num_sms / pl.C);
+  // split the vocabulary so the units spread evenly over the CTAs (one per
+  // SM): minimise ceil(units / CTAs) / splits (the time of the busiest CTA),
+  // keeping at least 8 blocks per split
+  const int64_t per_split = static_cast<int64_t>(pl.m_tiles) * pl.n_tiles;
+  const int ctas = std::max(1, num_sms);
   const int smax = std::max(1, std::min(64, pl.kblocks / 8));
   pl.splits = 1;
   double best = 1e30;
   for (int S = 1; S <= smax; ++S) {
-    const double cost = static_cast<double>((per_split * S + clusters - 1) / clusters) / S;
+    const double cost = static_cast<double>((per_split * S + ctas - 1) / ctas) / S;
     if (cost < best - 1e-12) {
       best = cost;
       pl.splits = S;
@@ -664,16 +610,15 @@ dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const
   if (st != DG_OK) return st;
   const ScPlan pl = sc_plan(rows, vocab, d_model, di->num_sms);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.total) return DG_ERR_WORKSPACE;
-  int ncl = di->sc_max_clusters[pl.C - 1];
-  if (ncl < 1) return DG_ERR_CUDA;
-  const int64_t units = static_cast<int64_t>(pl.splits) * pl.m_groups * pl.n_tiles;
-  if (units < ncl) ncl = static_cast<int>(units);
+  int ncta = di->num_sms;
+  const int64_t units = static_cast<int64_t>(pl.splits) * pl.m_tiles * pl.n_tiles;
+  if (units < ncta) ncta = static_cast<int>(units);
 
   CUtensorMap ml, me;
   // logits [rows, vocab]: boxes of 64 entries x 128 rows; E [vocab, d]: boxes
-  // of 64 columns x (64 / C) vocabulary rows
+  // of 64 columns x 64 vocabulary rows
   if (encode_map(&ml, logits, rows, 1, vocab, 1, kRows) != DG_OK ||
-      encode_map(&me, embedding, vocab, 1, d_model, 1, kScK / pl.C) != DG_OK)
+      encode_map(&me, embedding, vocab, 1, d_model, 1, kScK) != DG_OK)
     return DG_ERR_INVALID_ARG;
 
   uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -688,8 +633,9 @@ dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const
   p.d = d_model;
   p.m_tiles = pl.m_tiles;
   p.n_tiles = pl.n_tiles;
-  p.m_groups = pl.m_groups;
   p.splits = pl.splits;
+  p.debug_skip_e_load = -1;
+  if (const char* e = std::getenv("DG_SELFCOND_DEBUG_SKIP_E_LOAD")) p.debug_skip_e_load = std::atoi(e);
   p.kblocks = pl.kblocks;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -701,19 +647,8 @@ dg_status_t selfcond_impl(const void* logits, int32_t rows, int32_t vocab, const
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
   if (e0 && cudaEventRecord(e0, stream) != cudaSuccess) return DG_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ncl * pl.C);
-  cfg.blockDim = dim3(kScThreads);
-  cfg.dynamicSmemBytes = ScCfg::SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = pl.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, sc_kernel, ml, me, p) != cudaSuccess) return DG_ERR_CUDA;
+  sc_kernel<<<ncta, kScThreads, ScCfg::SMEM_BYTES, stream>>>(ml, me, p);
+  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   if (e1 && cudaEventRecord(e1, stream) != cudaSuccess) return DG_ERR_CUDA;
   if (pl.splits > 1) {
     const dim3 grid(pl.m_tiles, (d_model + 31) / 32);

@@ -1,18 +1,16 @@
 // Device side of the dual-mode attention forward pass.
 //
 //   build_worklist_kernel  one CTA: validates cu_q / ctx_len / mode, cuts every
-//                          (sequence, KV head) into 128-row query tiles, groups
-//                          C consecutive tiles (C = cluster size) and computes
-//                          each group's visible KV-tile range; the range is the
-//                          union of the rows' windows (causal: keys <= i,
-//                          bidirectional: the whole sequence, both narrowed to
-//                          [i-W, i+W] on sliding-window layers).
-//   fwd_kernel<D,BN,NK,NV> persistent, clusters of C CTAs.  The (group,
-//                          KV-tile) work units are split evenly over the
-//                          clusters; CTA r of a cluster owns query tile r of
-//                          the group, every CTA TMA-loads 1/C of each K/V tile
-//                          and multicasts it to the whole cluster.  A group
-//                          cut between clusters leaves fp32 partials + LSE.
+//                          (sequence, KV head) into 128-row query tiles and
+//                          computes each tile's visible KV-tile range; the
+//                          range is the union of the rows' windows (causal:
+//                          keys <= i, bidirectional: the whole sequence, both
+//                          narrowed to [i-W, i+W] on sliding-window layers).
+//   fwd_kernel<D,BN,NK,NV> persistent, one CTA per SM.  The (tile, KV-tile)
+//                          work units are split evenly over the CTAs; every
+//                          CTA TMA-loads the K/V tiles it consumes from this
+//                          GPU's memory into its own shared memory.  A tile cut
+//                          between CTAs leaves fp32 partials + LSE.
 //                          Warp roles: warps 4 and 6 issue TMA loads (K ring,
 //                          V ring), warp 5 issues tcgen05 MMAs, warps 0-3
 //                          (one TMEM lane = one query row each) stage Q in
@@ -24,8 +22,8 @@
 // the physical page of positions p*P .. p*P+P-1 of sequence s.  The work-list
 // launch then also appends the query tokens' K/V rows into their pages (CTAs
 // 1.. of the launch) and checks every page-table entry the attention will
-// read; the loaders look up each slice's page and load it in boxes of
-// min(P, BN / C) rows.
+// read; the loaders look up each tile's pages and load them in boxes of
+// min(P, BN) rows, one box per lane of the loader warp.
 //
 // Rules (DiffusionGemma, agentlenshq page, "dual-mode operation", "dynamic
 // per-sequence causal attention", "symmetric sliding-window attention"): a
@@ -51,30 +49,30 @@ constexpr int kMmaWarp = 5;         // issues tcgen05 MMAs, owns TMEM
 constexpr int kVLoadWarp = 6;       // loads the V ring
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitTimeoutNs = 250ull * 1000ull * 1000ull;
-constexpr int kMaxCluster = 8;      // portable cluster size limit
 // Work-split weight of starting a segment (Q load, pipeline fill, epilogue),
-// in KV-tile units: every group occupies kSegWeight + (its KV tiles) units of
+// in KV-tile units: every tile occupies kSegWeight + (its KV tiles) units of
 // the split, the first kSegWeight of them carrying no KV tile.
 constexpr int kSegWeight = 8;
 
 // error codes shared with the host (same values as dg_status_t)
 constexpr int kErrInvalid = 1;
 constexpr int kErrTimeout = 5;
+constexpr int kErrBounds = 6;
 
 struct TileDesc {
   int32_t q_row0;    // global query row of the tile's first token
-  int32_t n_tok;     // query tokens in the tile (1 .. TT; 0 = no tile for this cluster rank)
+  int32_t n_tok;     // query tokens in the tile (1 .. TT)
   int32_t kv_row0;   // global K/V row of the sequence's first key (paged: its page-table row offset)
   int32_t pos0;      // absolute position of the tile's first token
   int32_t L;         // keys of the sequence (context + queries)
-  int32_t kt_first;  // first KV tile of the group's range (units of BN keys, sequence-relative)
+  int32_t kt_first;  // first KV tile of the tile's range (units of BN keys, sequence-relative)
   int32_t kvh;       // KV head
   int32_t causal;    // 1 causal (encoder), 0 bidirectional (denoise)
-  int32_t kt_count;  // KV tiles in the group's range
-  int32_t kt_rot;    // the group's KV tiles are visited from kt_first + kt_rot on, cyclically
+  int32_t kt_count;  // KV tiles in the range
+  int32_t kt_rot;    // the KV tiles are visited from kt_first + kt_rot on, cyclically
 };
 
-// KV tile (sequence-relative, units of BN keys) visited j-th in a group.
+// KV tile (sequence-relative, units of BN keys) visited j-th for a query tile.
 __device__ __forceinline__ int kv_tile(const TileDesc& td, int j) {
   int x = j + td.kt_rot;
   if (x >= td.kt_count) x -= td.kt_count;
@@ -82,17 +80,17 @@ __device__ __forceinline__ int kv_tile(const TileDesc& td, int j) {
 }
 
 struct WorkHeader {
-  int32_t num_tiles;  // tile groups (one per cluster-wide work item)
+  int32_t num_tiles;  // query tiles
   int32_t error;
   int64_t total_units;
 };
 
 struct Workspace {
   WorkHeader* hdr;
-  int64_t* seq_tile_off;   // [B + 1] groups before each sequence
+  int64_t* seq_tile_off;   // [B + 1] tiles before each sequence
   int64_t* seq_kv_off;     // [B + 1]
-  TileDesc* tiles;         // [max_groups][C]: group g, cluster rank r at g * C + r
-  int64_t* unit_begin;     // [max_groups + 1]
+  TileDesc* tiles;         // [max_tiles]
+  int64_t* unit_begin;     // [max_tiles + 1]
   float* part_lse;         // [2 * num_ctas][128]
   float* part_o;           // [2 * num_ctas][128][D]
 };
@@ -103,7 +101,7 @@ struct FwdParams {
   __nv_bfloat16* out;
   float* lse;
   int* status;
-  int Hq, G, TT, window, C;
+  int Hq, G, TT, window;
   // paged KV cache: block_table [B, bt_stride] (nullptr: contiguous K/V),
   // pages of 2^page_shift rows, TMA boxes of page_box rows
   const int32_t* block_table;
@@ -111,6 +109,14 @@ struct FwdParams {
   // >= 0: the K loader skips the TMA load of this (per-CTA) KV tile, so the
   // MMA warp's bounded wait for it expires (tests of the timeout path)
   int debug_skip_k_load;
+  // sizes the bounds-checking build checks every index against: K/V rows of
+  // the tensor maps, KV heads, query rows, partial slots, page-table entries
+  int Hkv, kv_rows, total_q, num_slots;
+  int64_t bt_entries;
+  // bounds-checking build only, >= 0: the K loader moves the row coordinate
+  // of this (per-CTA) KV tile past the tensor, so its bounds check fails
+  // (tests of the check; the load it guards is skipped)
+  int debug_bad_kv_row;
   float scale, scale_log2;  // softmax scale (times the q and k scales for e4m3 inputs)
   float v_scale;            // e4m3 inputs: the v scale, applied in the epilogue (1 for bf16)
 };
@@ -147,6 +153,29 @@ __device__ __forceinline__ void store_packed_p(uint32_t taddr, const uint32_t (&
 
 __device__ __forceinline__ void record_error(int* status, int code) {
   atomicCAS(status, 0, code);
+}
+
+// Bounds checks of the debug build (compiled with DG_ATTN_DEBUG): every TMA
+// coordinate, shared-memory destination, TMEM column and global index is
+// checked against its buffer before the access.  A failed check records
+// DG_ERR_DEVICE_BOUNDS in the status word, raises the CTA's abort flag (every
+// role then leaves its loop through the bounded-wait exits) and the access is
+// skipped.  Release builds compile the checks out.
+#ifdef DG_ATTN_DEBUG
+constexpr bool kBoundsChecks = true;
+#else
+constexpr bool kBoundsChecks = false;
+#endif
+__device__ __forceinline__ bool in_bounds(bool ok, int* status, volatile int* abort_flag) {
+  if constexpr (kBoundsChecks) {
+    if (!ok) {
+      record_error(status, kErrBounds);
+      if (abort_flag != nullptr) *abort_flag = 1;
+    }
+    return ok;
+  } else {
+    return true;
+  }
 }
 
 // ------------------------------------------------------------ block scan
@@ -268,8 +297,8 @@ __device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int P) {
 __global__ void __launch_bounds__(1024, 1)
 build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ ctx_len,
                       const uint8_t* __restrict__ mode, int B, int total_q, int total_kv, int Hkv,
-                      int TT, int BN, int window, int max_groups, int C, int num_clusters,
-                      int rotate, Workspace ws, PagedArgs pg, int* status) {
+                      int TT, int BN, int window, int max_tiles, int num_ctas, int rotate,
+                      Workspace ws, PagedArgs pg, int* status) {
   // the attention kernel is launched as a programmatic dependent: its CTAs
   // become resident while this grid runs and wait for it to finish
   griddep_launch_dependents();
@@ -289,7 +318,7 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     if (n < 0 || c < 0 || md > 1) atomicOr(&bad, 1);
     const int64_t nn = n < 0 ? 0 : n;
     const int64_t m_tiles = (nn + TT - 1) / TT;
-    ws.seq_tile_off[s] = static_cast<int64_t>(Hkv) * ((m_tiles + C - 1) / C);
+    ws.seq_tile_off[s] = static_cast<int64_t>(Hkv) * m_tiles;
     ws.seq_kv_off[s] = static_cast<int64_t>(c < 0 ? 0 : c) + nn;
   }
   __syncthreads();
@@ -312,7 +341,7 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
   block_exclusive_scan(ws.seq_tile_off, B);
   block_exclusive_scan(ws.seq_kv_off, B);
   if (tid == 0) {
-    if (ws.seq_tile_off[B] > max_groups || (!paged && ws.seq_kv_off[B] > total_kv)) bad = 1;
+    if (ws.seq_tile_off[B] > max_tiles || (!paged && ws.seq_kv_off[B] > total_kv)) bad = 1;
   }
   __syncthreads();
   if (bad) {
@@ -325,12 +354,12 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     return;
   }
   const int num_tiles = static_cast<int>(ws.seq_tile_off[B]);
-  for (int grp = tid; grp < num_tiles; grp += 1024) {
-    // sequence owning this group: largest s with seq_tile_off[s] <= grp
+  for (int tile = tid; tile < num_tiles; tile += 1024) {
+    // sequence owning this tile: largest s with seq_tile_off[s] <= tile
     int lo = 0, hi = B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (ws.seq_tile_off[mid] <= grp) lo = mid; else hi = mid - 1;
+      if (ws.seq_tile_off[mid] <= tile) lo = mid; else hi = mid - 1;
     }
     const int s = lo;
     const int n = cu_q[s + 1] - cu_q[s];
@@ -338,34 +367,27 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     const int L = c + n;
     const bool causal = mode[s] == 0;
     const int m_tiles = (n + TT - 1) / TT;
-    const int n_groups = (m_tiles + C - 1) / C;
-    const int local = grp - static_cast<int>(ws.seq_tile_off[s]);
-    const int kvh = local / n_groups;
-    const int gi = local - kvh * n_groups;
-    const int mt0 = gi * C;
-    const int mt_last = min(m_tiles, mt0 + C) - 1;
-    const int pos_first = c + mt0 * TT;
-    const int i_max = c + min(n, (mt_last + 1) * TT) - 1;
+    const int local = tile - static_cast<int>(ws.seq_tile_off[s]);
+    const int kvh = local / m_tiles;
+    const int mt = local - kvh * m_tiles;
+    const int t0 = mt * TT;
+    const int pos_first = c + t0;
+    const int i_max = c + min(n, t0 + TT) - 1;
     const int kv_lo = window < 0 ? 0 : max(0, pos_first - window);
     const int kv_hi = causal ? i_max : (window < 0 ? L - 1 : min(L - 1, i_max + window));
-    for (int r = 0; r < C; ++r) {
-      const int mt = mt0 + r;
-      const bool present = mt <= mt_last;
-      const int t0 = (present ? mt : mt0) * TT;
-      TileDesc td;
-      td.q_row0 = cu_q[s] + t0;
-      td.n_tok = present ? min(TT, n - t0) : 0;
-      td.kv_row0 = paged ? s * pg.bt_stride : static_cast<int>(ws.seq_kv_off[s]);
-      td.pos0 = c + t0;
-      td.L = L;
-      td.kt_first = kv_lo / BN;
-      td.kvh = kvh;
-      td.causal = causal ? 1 : 0;
-      td.kt_count = kv_hi / BN - kv_lo / BN + 1;
-      td.kt_rot = 0;
-      ws.tiles[static_cast<size_t>(grp) * C + r] = td;
-    }
-    ws.unit_begin[grp] = kSegWeight + kv_hi / BN - kv_lo / BN + 1;
+    TileDesc td;
+    td.q_row0 = cu_q[s] + t0;
+    td.n_tok = min(TT, n - t0);
+    td.kv_row0 = paged ? s * pg.bt_stride : static_cast<int>(ws.seq_kv_off[s]);
+    td.pos0 = pos_first;
+    td.L = L;
+    td.kt_first = kv_lo / BN;
+    td.kvh = kvh;
+    td.causal = causal ? 1 : 0;
+    td.kt_count = kv_hi / BN - kv_lo / BN + 1;
+    td.kt_rot = 0;
+    ws.tiles[tile] = td;
+    ws.unit_begin[tile] = kSegWeight + td.kt_count;
   }
   __syncthreads();
   block_exclusive_scan(ws.unit_begin, num_tiles);
@@ -375,24 +397,23 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     ws.hdr->error = 0;
   }
   if (!rotate) return;
-  // KV visiting order.  The clusters' unit ranges are contiguous and equally
-  // long (U / P units), so the clusters sharing one group start at KV-tile
-  // offsets a multiple of U / P apart.  Rotating each group's tiles so that
-  // the cluster holding its first tile reaches that tile at "time" (units
-  // since the launch) equal to the tile index gives every cluster of every
-  // group a phase that is a multiple of U / P: the groups of one (sequence,
-  // KV head) with the same KV range then stream the same KV tiles at about
-  // the same time, and the later readers find them in L2.  The order of the
-  // tiles does not change the result beyond fp32 rounding.
+  // KV visiting order.  The CTAs' unit ranges are contiguous and equally
+  // long (U / P units), so the CTAs sharing one query tile start at KV-tile
+  // offsets a multiple of U / P apart.  Rotating each tile's KV tiles so that
+  // the CTA holding its first KV tile reaches that KV tile at "time" (units
+  // since the launch) equal to the KV tile's index gives every CTA of every
+  // query tile a phase that is a multiple of U / P: the query tiles of one
+  // (sequence, KV head) with the same KV range then stream the same KV tiles
+  // at about the same time, and the later readers find them in L2.  The
+  // order of the KV tiles does not change the result beyond fp32 rounding.
   const int64_t U = ws.unit_begin[num_tiles];
-  const int P = active_ctas(num_clusters, U);
-  for (int grp = tid; grp < num_tiles; grp += 1024) {
-    const int64_t r0 = ws.unit_begin[grp] + kSegWeight;
-    const int64_t n = ws.unit_begin[grp + 1] - r0;
+  const int P = active_ctas(num_ctas, U);
+  for (int tile = tid; tile < num_tiles; tile += 1024) {
+    const int64_t r0 = ws.unit_begin[tile] + kSegWeight;
+    const int64_t n = ws.unit_begin[tile + 1] - r0;
     if (n <= 1 || P <= 1) continue;
     const int64_t lead = r0 - cta_unit_begin(cta_of_unit(r0, U, P), U, P);  // >= 0
-    const int rot = static_cast<int>(lead % n);
-    for (int r = 0; r < C; ++r) ws.tiles[static_cast<size_t>(grp) * C + r].kt_rot = rot;
+    ws.tiles[tile].kt_rot = static_cast<int>(lead % n);
   }
 }
 
@@ -408,14 +429,14 @@ __device__ __forceinline__ int tile_of_unit(const int64_t* ub, int num_tiles, in
 
 struct Seg {
   int tile;
-  int j0, j1;   // KV-tile range within the group's range
-  int whole;    // segment covers every KV tile of its group
+  int j0, j1;   // KV-tile range within the tile's range
+  int whole;    // segment covers every KV tile of its query tile
   int slot;     // partial slot when not whole
 };
 
-// Walks the segments of one cluster's unit range; every role walks the same
-// list.  A group spans units [ub[g], ub[g+1]); its KV tiles are the units from
-// ub[g] + kSegWeight on, so a range that only touches a group's first
+// Walks the segments of one CTA's unit range; every role walks the same
+// list.  A query tile spans units [ub[t], ub[t+1]); its KV tiles are the units
+// from ub[t] + kSegWeight on, so a range that only touches a tile's first
 // kSegWeight units yields no segment of it.
 struct SegIter {
   const int64_t* ub;
@@ -523,9 +544,9 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
   // barriers
-  // S_FULL[s]: QK^T of the tile in K stage s is done in every CTA of the
-  // cluster (which also frees that K stage); O_DONE[s]: likewise P.V of the
-  // tile in V stage s (which frees that V stage)
+  // S_FULL[s]: QK^T of the tile in K stage s is done (which also frees that
+  // K stage); O_DONE[s]: likewise P.V of the tile in V stage s (which frees
+  // that V stage)
   // (with soft release, K_EMPTY / V_EMPTY free the stages instead)
   static constexpr int B_Q_FULL = 0, B_K_FULL = 1, B_V_FULL = 1 + NK,
                        B_S_FULL = 1 + NK + NV, B_P_FULL = B_S_FULL + NK,
@@ -568,20 +589,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   const WorkHeader* hdr = p.ws.hdr;
   const int num_tiles = hdr->num_tiles;
   const int64_t U = hdr->total_units;
-  const int C = static_cast<int>(cluster_size());
-  const int rank = static_cast<int>(cluster_cta_rank());
-  const int cl = static_cast<int>(cluster_index());
+  const int cta = static_cast<int>(blockIdx.x);
   if (num_tiles <= 0 || U <= 0) return;  // uniform over the grid
-  const int P = active_ctas(static_cast<int>(cluster_count()), U);
-  if (cl >= P) return;  // uniform over the cluster
-  const int64_t u_beg = cta_unit_begin(cl, U, P);
-  const int64_t u_end = cta_unit_begin(cl + 1, U, P);
-  const uint16_t cta_mask = static_cast<uint16_t>((1u << C) - 1u);
-  // Soft release (64-key tiles, no cluster): a softmax thread frees the K and
-  // V stages with an arrive once it has seen S(g), so the loaders wait on
-  // K_EMPTY / V_EMPTY; measured 1.5% faster there than freeing them through
-  // the MMA warp's S_FULL / O_DONE commits, which the other shapes use.
-  const bool soft_release = (BN == 64) && (C == 1);
+  const int P = active_ctas(static_cast<int>(gridDim.x), U);
+  if (cta >= P) return;  // uniform over the CTA
+  const int64_t u_beg = cta_unit_begin(cta, U, P);
+  const int64_t u_end = cta_unit_begin(cta + 1, U, P);
+  // Soft release (64-key tiles): a softmax thread frees the K and V stages
+  // with an arrive once it has seen S(g), so the loaders wait on K_EMPTY /
+  // V_EMPTY; measured 1.5% faster there than freeing them through the MMA
+  // warp's S_FULL / O_DONE commits, which the 128-key tiles use.
+  constexpr bool soft_release = (BN == 64);
 
   const uint32_t sK = sbase + Cf::OFF_K;
   const uint32_t sV = sbase + Cf::OFF_V;
@@ -592,18 +610,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Cf::B_Q_FULL), kRows);
-    // S_FULL / O_DONE count one commit from the MMA warp of every CTA of the
-    // cluster (multicast).  Tile g uses S_FULL[g % NK] and O_DONE[g % NV]: a
-    // wait for tile x never aliases, since the next tile on the same barrier,
-    // x + NK (x + NV), cannot be issued before P(x) exists.
+    // S_FULL / O_DONE count one commit from the MMA warp.  Tile g uses
+    // S_FULL[g % NK] and O_DONE[g % NV]: a wait for tile x never aliases,
+    // since the next tile on the same barrier, x + NK (x + NV), cannot be
+    // issued before P(x) exists.
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(Cf::B_K_FULL + s), 1);
-      mbar_init(bar(Cf::B_S_FULL + s), C);
+      mbar_init(bar(Cf::B_S_FULL + s), 1);
       mbar_init(bar(Cf::B_K_EMPTY + s), 1);
     }
     for (int s = 0; s < NV; ++s) {
       mbar_init(bar(Cf::B_V_FULL + s), 1);
-      mbar_init(bar(Cf::B_O_DONE + s), C);
+      mbar_init(bar(Cf::B_O_DONE + s), 1);
       mbar_init(bar(Cf::B_V_EMPTY + s), 1);
     }
     // one P_FULL per S/P buffer in TMEM: tile g uses index g & 1
@@ -627,96 +645,106 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (C > 1) cluster_sync_all();  // peers' barriers exist before any multicast
+  // all 512 columns of all 128 lanes: the column offsets below are compile-time
+  // constants within that range (checked by FwdCfg's static_asserts)
+  in_bounds(tmem == 0u, p.status, abort_flag);
 
-  SegIter it{p.ws.unit_begin, num_tiles, u_beg, u_end, cl * C + rank, true};
+  SegIter it{p.ws.unit_begin, num_tiles, u_beg, u_end, cta, true};
   const int G = p.G, TT = p.TT;
 
   if (warp == kTmaWarp || warp == kVLoadWarp) {
     // ----------------------------------------------------------- producers
-    // warp 4 loads the K ring, warp 6 the V ring; each CTA of a cluster loads
-    // BN / C rows of every tile and multicasts them to the whole cluster
-    if (lane == 0) {
-      const bool is_k = (warp == kTmaWarp);
-      const uint32_t t_tx = static_cast<uint32_t>(Cf::NKB * 64 * BN * 2);  // all C slices
-      const int slice = BN / C;                                               // rows per CTA
-      const int NS = is_k ? NK : NV;
-      const uint32_t full0 = bar(is_k ? Cf::B_K_FULL : Cf::B_V_FULL);
-      // a stage is free once its tile's QK^T (K) or P.V (V) is done in every CTA
-      const uint32_t empty0 = soft_release ? bar(is_k ? Cf::B_K_EMPTY : Cf::B_V_EMPTY)
-                                           : bar(is_k ? Cf::B_S_FULL : Cf::B_O_DONE);
-      const uint32_t ring = is_k ? sK : sV;
-      const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
-      uint32_t stage = 0, phase = 0;
-      uint32_t issued_mask = 0, issued_phase = 0;  // per stage: a load was issued / its phase
-      int loads = 0;
-      bool ok = true;
-      Seg sg;
-      while (ok && it.next(sg)) {
-        const TileDesc td = p.ws.tiles[static_cast<size_t>(sg.tile) * C + rank];
-        if (is_k) {
-          // the next segment's Q rows go to L2 while this segment streams, so
-          // the softmax warps load them at L2 latency at the segment switch
-          SegIter look = it;
-          Seg nx;
-          if (look.next(nx)) {
-            const TileDesc tn = p.ws.tiles[static_cast<size_t>(nx.tile) * C + rank];
-            const int ntok = max(tn.n_tok, 1);
-            for (int t = 0; t < ntok; ++t)
-              prefetch_l2_bulk(static_cast<const uint8_t*>(p.q) +
-                                   (static_cast<size_t>(tn.q_row0 + t) * p.Hq + tn.kvh * G) * D * E::SIZE,
-                               static_cast<uint32_t>(G * D * E::SIZE));
-          }
+    // Warp 4 loads the K ring, warp 6 the V ring, each from this GPU's
+    // memory into this CTA's shared memory.  The whole warp runs the loop
+    // with warp-uniform control flow; the TMA boxes of one KV tile are spread
+    // over the lanes, one box per lane, so that a paged tile's page lookups
+    // and box issues run side by side instead of one after the other.
+    const bool is_k = (warp == kTmaWarp);
+    const bool paged = p.block_table != nullptr;
+    const int NS = is_k ? NK : NV;
+    const uint32_t full0 = bar(is_k ? Cf::B_K_FULL : Cf::B_V_FULL);
+    // a stage is free once its tile's QK^T (K) or P.V (V) is done
+    const uint32_t empty0 = soft_release ? bar(is_k ? Cf::B_K_EMPTY : Cf::B_V_EMPTY)
+                                         : bar(is_k ? Cf::B_S_FULL : Cf::B_O_DONE);
+    const uint32_t ring = is_k ? sK : sV;
+    const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
+    // boxes of a tile: (BN / box_rows) row blocks x NKB 128-byte column blocks
+    // (at most 32: a box holds at least 8 rows, BN * NKB <= 256)
+    const int box_rows = paged ? p.page_box : BN;
+    const int nbr = BN / box_rows;
+    const bool has_box = lane < nbr * Cf::NKB;
+    const int br = lane % nbr, bk = lane / nbr;
+    const uint32_t box_off = static_cast<uint32_t>(bk * (BN * 128) + br * box_rows * 128);
+    const int pmask = (1 << p.page_shift) - 1;
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_mask = 0, issued_phase = 0;  // per stage: a load was issued / its phase
+    int loads = 0;
+    bool ok = true;
+    Seg sg;
+    while (ok && it.next(sg)) {
+      const TileDesc td = p.ws.tiles[sg.tile];
+      if (is_k) {
+        // the next segment's Q rows go to L2 while this segment streams, so
+        // the softmax warps load them at L2 latency at the segment switch
+        SegIter look = it;
+        Seg nx;
+        if (look.next(nx)) {
+          const TileDesc tn = p.ws.tiles[nx.tile];
+          for (int t = lane; t < tn.n_tok; t += 32)
+            prefetch_l2_bulk(static_cast<const uint8_t*>(p.q) +
+                                 (static_cast<size_t>(tn.q_row0 + t) * p.Hq + tn.kvh * G) * D * E::SIZE,
+                             static_cast<uint32_t>(G * D * E::SIZE));
         }
-        for (int j = sg.j0; j < sg.j1; ++j) {
-          if (!wait_phase(empty0 + 8u * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
-          if (is_k && loads++ == p.debug_skip_k_load) {
-            if (++stage == static_cast<uint32_t>(NS)) { stage = 0; phase ^= 1; }
-            continue;
-          }
-          mbar_arrive_expect_tx(full0 + 8u * stage, t_tx);
-          const uint32_t dst = ring + stage * Cf::KV_BYTES + rank * slice * 128;
-          if (p.block_table == nullptr) {
-            const int row = td.kv_row0 + kv_tile(td, j) * BN + rank * slice;
-#pragma unroll
-            for (int kb = 0; kb < Cf::NKB; ++kb) {
-              if (C > 1)
-                tma_load_3d_multicast(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * E::BLK, td.kvh,
-                                      row, cta_mask);
-              else
-                tma_load_3d(dst + kb * (BN * 128), map, full0 + 8u * stage, kb * E::BLK, td.kvh, row);
-            }
-          } else {
-            // positions past the sequence's last key read its last page
-            // (checked by the work-list launch); the softmax masks them
-            const int pos0 = kv_tile(td, j) * BN + rank * slice;
-            const int last_page = (td.L - 1) >> p.page_shift;
-            const int pmask = (1 << p.page_shift) - 1;
-            for (int r0 = 0; r0 < slice; r0 += p.page_box) {
-              const int pos = pos0 + r0;
-              const int page = __ldg(p.block_table + td.kv_row0 + min(pos >> p.page_shift, last_page));
-              const int row = (page << p.page_shift) + (pos & pmask);
-              const uint32_t d0 = dst + r0 * 128;
-#pragma unroll
-              for (int kb = 0; kb < Cf::NKB; ++kb) {
-                if (C > 1)
-                  tma_load_3d_multicast(d0 + kb * (BN * 128), map, full0 + 8u * stage, kb * E::BLK, td.kvh,
-                                        row, cta_mask);
-                else
-                  tma_load_3d(d0 + kb * (BN * 128), map, full0 + 8u * stage, kb * E::BLK, td.kvh, row);
-              }
-            }
-          }
-          issued_mask |= 1u << stage;
-          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+      }
+      // positions past the sequence's last key read its last page (checked
+      // by the work-list launch); the softmax masks them
+      const int last_page = (td.L - 1) >> p.page_shift;
+      for (int j = sg.j0; j < sg.j1; ++j) {
+        if (!__all_sync(0xffffffffu, wait_phase(empty0 + 8u * stage, phase ^ 1, abort_flag, p.status))) {
+          ok = false;
+          break;
+        }
+        if (is_k && loads++ == p.debug_skip_k_load) {
           if (++stage == static_cast<uint32_t>(NS)) { stage = 0; phase ^= 1; }
+          continue;
         }
+        // the expected bytes are registered before any box of the stage is issued
+        if (lane == 0) mbar_arrive_expect_tx(full0 + 8u * stage, static_cast<uint32_t>(Cf::KV_BYTES));
+        __syncwarp();
+        if (has_box) {
+          const int pos = kv_tile(td, j) * BN + br * box_rows;
+          int row;
+          bool ok_box = true;
+          if (!paged) {
+            row = td.kv_row0 + pos;
+          } else {
+            const int64_t ent = static_cast<int64_t>(td.kv_row0) + min(pos >> p.page_shift, last_page);
+            ok_box = in_bounds(ent >= 0 && ent < p.bt_entries, p.status, abort_flag);
+            const int page = ok_box ? __ldg(p.block_table + ent) : 0;
+            row = (page << p.page_shift) + (pos & pmask);
+          }
+          if constexpr (kBoundsChecks) {
+            if (is_k && loads - 1 == p.debug_bad_kv_row) row += p.kv_rows;
+          }
+          const uint32_t dst = ring + stage * Cf::KV_BYTES + box_off;
+          // a box starts inside the tensor (its rows past the end are zero-filled
+          // by the TMA unit and masked) and lands inside its ring stage
+          ok_box = ok_box &&
+                   in_bounds(row >= 0 && row < p.kv_rows && td.kvh >= 0 && td.kvh < p.Hkv &&
+                                 (bk + 1) * E::BLK <= D && (dst & 1023u) == 0u &&
+                                 dst + static_cast<uint32_t>(box_rows * 128) <= ring + NS * Cf::KV_BYTES,
+                             p.status, abort_flag);
+          if (ok_box) tma_load_3d(dst, map, full0 + 8u * stage, bk * E::BLK, td.kvh, row);
+        }
+        issued_mask |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == static_cast<uint32_t>(NS)) { stage = 0; phase ^= 1; }
       }
-      if (!ok) {
-        // let loads already in flight land before the CTA's shared memory goes away
-        for (int st = 0; st < NS; ++st)
-          if (issued_mask & (1u << st)) drain_wait(full0 + 8u * st, (issued_phase >> st) & 1);
-      }
+    }
+    if (!ok) {
+      // let loads already in flight land before the CTA's shared memory goes away
+      for (int st = 0; st < NS; ++st)
+        if (issued_mask & (1u << st)) drain_wait(full0 + 8u * st, (issued_phase >> st) & 1);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -762,8 +790,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
               if constexpr (F8) umma_e4m3_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
               else umma_bf16_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            if (C > 1) umma_commit_multicast_warp(bar(Cf::B_S_FULL + k_stage), cta_mask);
-            else umma_commit_warp(bar(Cf::B_S_FULL + k_stage));
+            umma_commit_warp(bar(Cf::B_S_FULL + k_stage));
             if (++k_stage == NK) { k_stage = 0; k_phase ^= 1; }
           }
           if (jj >= 1) {
@@ -790,8 +817,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
               else
                 umma_bf16_ts_warp(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
             }
-            if (C > 1) umma_commit_multicast_warp(bar(Cf::B_O_DONE + v_stage), cta_mask);
-            else umma_commit_warp(bar(Cf::B_O_DONE + v_stage));
+            umma_commit_warp(bar(Cf::B_O_DONE + v_stage));
             if (++v_stage == NV) { v_stage = 0; v_phase ^= 1; }
           }
         }
@@ -820,12 +846,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // this segment's epilogue and land while O is drained.
     constexpr int kQW = D / E::PER_WORD;  // packed 32-bit words of a Q row
     uint32_t qw[kQW];
+    // (rows past the tile's tokens load the last token's row; they write nothing)
     auto q_issue = [&](const TileDesc& t) {
-      const int ntq = max(t.n_tok, 1);
       const int hq = t.kvh * G + (r < G * TT ? g_row : 0);
+      const int qr = t.q_row0 + min(t_row, t.n_tok - 1);
+      const bool q_ok = in_bounds(qr >= 0 && qr < p.total_q && hq >= 0 && hq < p.Hq, p.status, abort_flag);
       const uint4* src = reinterpret_cast<const uint4*>(
-          static_cast<const uint8_t*>(p.q) +
-          (static_cast<size_t>(t.q_row0 + min(t_row, ntq - 1)) * p.Hq + hq) * D * E::SIZE);
+          static_cast<const uint8_t*>(p.q) + (static_cast<size_t>(q_ok ? qr : 0) * p.Hq + (q_ok ? hq : 0)) *
+                                                 D * E::SIZE);
 #pragma unroll
       for (int e = 0; e < kQW / 4; ++e) {
         const uint4 x = __ldg(src + e);
@@ -843,7 +871,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     Seg sg;
     bool have = it.next(sg);
     if (have) {
-      q_issue(p.ws.tiles[static_cast<size_t>(sg.tile) * C + rank]);
+      q_issue(p.ws.tiles[sg.tile]);
       q_commit();
     }
     // With head_dim 256 the register file has room to stage the next row
@@ -851,15 +879,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     constexpr bool kStageQ = (D == 256);
     bool q_loaded = true;  // the first segment's Q is already in TMEM
     while (ok && have) {
-      const TileDesc td = p.ws.tiles[static_cast<size_t>(sg.tile) * C + rank];
+      const TileDesc td = p.ws.tiles[sg.tile];
       if (!q_loaded) {
         q_issue(td);
         q_commit();
       }
-      // a rank without a tile in this group (n_tok == 0) still runs the
-      // pipeline on its neighbour's rows so the cluster stays in lockstep,
-      // but writes nothing
-      const int nt = max(td.n_tok, 1);
+      const int nt = td.n_tok;
       const bool row_ok = (t_row < TT) && (t_row < td.n_tok);
       const int tq = min(t_row, nt - 1);
       const int i = td.pos0 + tq;
@@ -970,19 +995,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       Seg nx;
       SegIter look = it;
       const bool more = kStageQ && look.next(nx);
-      if (more) q_issue(p.ws.tiles[static_cast<size_t>(nx.tile) * C + rank]);
+      if (more) q_issue(p.ws.tiles[nx.tile]);
       const float inv_l = l_run > 0.f ? p.v_scale / l_run : 0.f;
       // l_run sums the probabilities scaled by 2^P_SHIFT
       const float lse_v = l_run > 0.f ? m_run * p.scale + logf(l_run) - E::P_SHIFT * 0.6931471805599453f
                                       : -INFINITY;
       if (sg.whole) {
         const int orow = td.q_row0 + t_row;
+        const bool w_ok = !row_ok || in_bounds(orow >= 0 && orow < p.total_q && td.kvh * G + g_row < p.Hq,
+                                               p.status, abort_flag);
         __nv_bfloat16* dst = p.out + (static_cast<size_t>(orow) * p.Hq + td.kvh * G + g_row) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(lane_base + Cf::TM_O + c * 32, o);
-          if (row_ok) {
+          if (row_ok && w_ok) {
             uint32_t w[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
@@ -992,21 +1019,24 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
           }
         }
-        if (row_ok && p.lse != nullptr)
+        if (row_ok && w_ok && p.lse != nullptr)
           p.lse[static_cast<size_t>(orow) * p.Hq + td.kvh * G + g_row] = lse_v;
       } else {
+        const bool s_ok = in_bounds(sg.slot >= 0 && sg.slot < p.num_slots, p.status, abort_flag);
         float* dst = p.ws.part_o + (static_cast<size_t>(sg.slot) * kRows + r) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(lane_base + Cf::TM_O + c * 32, o);
           float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+          if (s_ok) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            d4[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
-                                __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l);
+            for (int e = 0; e < 8; ++e)
+              d4[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
+                                  __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l);
+          }
         }
-        p.ws.part_lse[static_cast<size_t>(sg.slot) * kRows + r] = lse_v;
+        if (s_ok) p.ws.part_lse[static_cast<size_t>(sg.slot) * kRows + r] = lse_v;
       }
       if (more) q_commit();
       tc_fence_before();
@@ -1024,8 +1054,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // no CTA leaves while a peer may still multicast into its shared memory
-  if (C > 1) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ combine
@@ -1035,19 +1063,17 @@ constexpr int kCombineWarps = 8;
 
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
-combine_kernel(const FwdParams p, int num_clusters) {
+combine_kernel(const FwdParams p, int num_ctas) {
   const WorkHeader* hdr = p.ws.hdr;
-  const int C = p.C;
-  const int grp = blockIdx.x / C, rank = blockIdx.x - grp * C;
-  if (grp >= hdr->num_tiles) return;
+  const int tile = blockIdx.x;
+  if (tile >= hdr->num_tiles) return;
   const int64_t U = hdr->total_units;
-  const int P = active_ctas(num_clusters, U);
-  const int64_t T0 = p.ws.unit_begin[grp], T1 = p.ws.unit_begin[grp + 1];
-  const int c_lo = cta_of_unit(T0 + kSegWeight, U, P);  // clusters holding KV tiles of the group
+  const int P = active_ctas(num_ctas, U);
+  const int64_t T0 = p.ws.unit_begin[tile], T1 = p.ws.unit_begin[tile + 1];
+  const int c_lo = cta_of_unit(T0 + kSegWeight, U, P);  // CTAs holding KV tiles of the tile
   const int c_hi = cta_of_unit(T1 - 1, U, P);
-  if (c_lo == c_hi) return;  // written directly by one cluster
-  const TileDesc td = p.ws.tiles[blockIdx.x];
-  if (td.n_tok == 0) return;
+  if (c_lo == c_hi) return;  // written directly by one CTA
+  const TileDesc td = p.ws.tiles[tile];
   const int G = p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * kCombineWarps + warp;
@@ -1055,15 +1081,17 @@ combine_kernel(const FwdParams p, int num_clusters) {
   const int t = r / G, gi = r - t * G;
   if (t >= td.n_tok) return;
   const int nc = c_hi - c_lo + 1;
-  auto slot_of = [&](int c) {
-    const int cta = c * C + rank;
-    return cta_unit_begin(c, U, P) >= T0 ? 2 * cta : 2 * cta + 1;
-  };
+  // a CTA's first segment uses slot 2c, its later one 2c + 1
+  auto slot_of = [&](int c) { return cta_unit_begin(c, U, P) >= T0 ? 2 * c : 2 * c + 1; };
   // the partials are written by the attention grid, this grid's predecessor
   griddep_wait();
   constexpr int E = D / 32;  // columns per lane
   const int orow = td.q_row0 + t;
   const int h = td.kvh * G + gi;
+  // every partial slot this row reads and the row it writes
+  if (!in_bounds(orow >= 0 && orow < p.total_q && h < p.Hq && c_lo >= 0 && slot_of(c_hi) < p.num_slots,
+                 p.status, nullptr))
+    return;
   __nv_bfloat16* dst = p.out + (static_cast<size_t>(orow) * p.Hq + h) * D;
   if (nc <= 4) {
     // the usual case: every load of the row (up to four contributors' LSE and

@@ -82,17 +82,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
       : "memory");
 }
 
-// Same, delivered to the same shared-memory offset (data and mbarrier) of every
-// CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const void* map, uint32_t bar,
-                                                      int c0, int c1, int c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
-      : "memory");
-}
-
 // ------------------------------------------- programmatic dependent launch
 // Dependent grid: wait until the preceding grid has completed and its writes
 // are visible.  Preceding grid: allow the dependent grid to start launching
@@ -100,34 +89,6 @@ __device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const void* 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// ------------------------------------------------------------------ cluster
-__device__ __forceinline__ uint32_t cluster_cta_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_index() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-// All threads of every CTA of the cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) of global
@@ -201,16 +162,6 @@ __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
-// Same, arriving on the mbarrier at this offset in every CTA named in cta_mask.
-__device__ __forceinline__ void umma_commit_multicast_warp(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n\t}" ::"r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // Shared-memory matrix descriptor, 128-byte swizzle (8-row x 128-byte atoms
 // that start on 1024-byte boundaries).  lbo/sbo in bytes.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {

@@ -9,15 +9,15 @@
 //       constant c_r = m_r log2(e) + log2(s_r) of its softmax, so that
 //       p = 2^(x log2(e) - c_r) needs one FMA and one ex2 per logit.
 //   sc_kernel: a persistent tcgen05 GEMM.  Work units are (vocabulary split,
-//       group of C row tiles, 256-column tile of E); clusters take units
-//       round-robin with the split outermost, so the clusters running at any
-//       moment read the same vocabulary range of logits and E and share it
-//       in L2.  Per 64-entry vocabulary block: TMA brings the 128 x 64 logits
-//       tile of this CTA's rows and 1/C of the 64 x 256 E tile (multicast to
-//       the cluster); several warps per TMEM lane quadrant (one row and a
-//       share of the block's columns per thread) turn the logits into bf16
-//       probabilities written straight to TMEM; the MMA warp accumulates
-//       P (A from TMEM) x E (B, N-major in shared memory) into TMEM.
+//       128-row tile, 256-column tile of E); CTAs take units round-robin with
+//       the split outermost, so the CTAs running at any moment read the same
+//       vocabulary range of logits and E and share it in L2.  Per 64-entry
+//       vocabulary block: TMA brings the 128 x 64 logits tile of this CTA's
+//       rows and the 64 x 256 E tile into this CTA's shared memory; several
+//       warps per TMEM lane quadrant (one row and a share of the block's
+//       columns per thread) turn the logits into bf16 probabilities written
+//       straight to TMEM; the MMA warp accumulates P (A from TMEM) x E (B,
+//       N-major in shared memory) into TMEM.
 //   sc_combine_kernel: sums the splits' fp32 partials when there are several.
 #pragma once
 
@@ -67,8 +67,11 @@ struct ScParams {
   float* part;        // splits > 1: fp32 [splits, m_tiles, n_tiles, kScN, 128], each
                       // tile column-major so the epilogue's stores coalesce
   int* status;
+  // >= 0: the E loader skips its load of this (per-CTA) block, so the MMA
+  // warp's bounded wait for it expires (tests of the timeout path)
+  int debug_skip_e_load;
   int rows, vocab, d;
-  int m_tiles, n_tiles, m_groups, splits, kblocks;
+  int m_tiles, n_tiles, splits, kblocks;
 };
 
 // a thread's packed probabilities -> TMEM (8 or 16 columns, by share size)
@@ -79,15 +82,14 @@ struct ScUnit {
   int split, mt, nt, kb0, kb1;
 };
 
-// Unit u: split outermost, then the group of C row tiles, then the E tile.
-__device__ __forceinline__ ScUnit sc_unit(const ScParams& p, int64_t u, int C, int rank) {
-  const int64_t per_split = static_cast<int64_t>(p.m_groups) * p.n_tiles;
+// Unit u: split outermost, then the row tile, then the E tile.
+__device__ __forceinline__ ScUnit sc_unit(const ScParams& p, int64_t u) {
+  const int64_t per_split = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   ScUnit w;
   w.split = static_cast<int>(u / per_split);
   const int rem = static_cast<int>(u - w.split * per_split);
-  const int mg = rem / p.n_tiles;
-  w.nt = rem - mg * p.n_tiles;
-  w.mt = mg * C + rank;
+  w.mt = rem / p.n_tiles;
+  w.nt = rem - w.mt * p.n_tiles;
   w.kb0 = static_cast<int>(static_cast<int64_t>(w.split) * p.kblocks / p.splits);
   w.kb1 = static_cast<int>(static_cast<int64_t>(w.split + 1) * p.kblocks / p.splits);
   return w;
@@ -128,12 +130,9 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int C = static_cast<int>(cluster_size());
-  const int rank = static_cast<int>(cluster_cta_rank());
-  const int cl = static_cast<int>(cluster_index());
-  const int ncl = static_cast<int>(cluster_count());
-  const int64_t U = static_cast<int64_t>(p.splits) * p.m_groups * p.n_tiles;
-  const uint16_t cta_mask = static_cast<uint16_t>((1u << C) - 1u);
+  const int cl = static_cast<int>(blockIdx.x);
+  const int ncl = static_cast<int>(gridDim.x);
+  const int64_t U = static_cast<int64_t>(p.splits) * p.m_tiles * p.n_tiles;
 
   const uint32_t sL = sbase + Cf::OFF_L;
   const uint32_t sE = sbase + Cf::OFF_E;
@@ -147,10 +146,9 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
       mbar_init(bar(Cf::B_L_FULL + s), 1);
       mbar_init(bar(Cf::B_L_EMPTY + s), kScXform);
     }
-    // an E slot is free once every CTA of the cluster has consumed it
     for (int s = 0; s < kScNE; ++s) {
       mbar_init(bar(Cf::B_E_FULL + s), 1);
-      mbar_init(bar(Cf::B_E_EMPTY + s), C);
+      mbar_init(bar(Cf::B_E_EMPTY + s), 1);
     }
     for (int s = 0; s < kScNP; ++s) {
       mbar_init(bar(Cf::B_P_FULL + s), kScXform);
@@ -175,41 +173,45 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (C > 1) cluster_sync_all();  // peers' barriers exist before any multicast
 
   if (warp == kTmaWarp || warp == kVLoadWarp) {
     // ----------------------------------------------------------- producers
-    // warp 4 loads this CTA's logits tiles, warp 6 its 1/C slice of every E
-    // tile, multicast to the cluster
+    // warp 4 loads this CTA's logits tiles, warp 6 its E tiles, both from
+    // this GPU's memory into this CTA's shared memory
     if (lane == 0) {
       const bool is_l = (warp == kTmaWarp);
       const int NS = is_l ? kScNL : kScNE;
       const uint32_t full0 = bar(is_l ? Cf::B_L_FULL : Cf::B_E_FULL);
       const uint32_t empty0 = bar(is_l ? Cf::B_L_EMPTY : Cf::B_E_EMPTY);
-      const int slice = kScK / C;  // E rows this CTA loads
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;
+      int loads = 0;
       bool ok = true;
       for (int64_t u = cl; ok && u < U; u += ncl) {
-        const ScUnit w = sc_unit(p, u, C, rank);
+        const ScUnit w = sc_unit(p, u);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!wait_phase(empty0 + 8u * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!is_l && loads++ == p.debug_skip_e_load) {
+            // test hook: this stage is never filled, so the MMA warp's
+            // bounded wait for it expires
+            if (++stage == static_cast<uint32_t>(NS)) { stage = 0; phase ^= 1; }
+            continue;
+          }
+          // (bounds-checking build) every box starts inside its tensor
           if (is_l) {
             mbar_arrive_expect_tx(full0 + 8u * stage, Cf::L_BYTES);
-            tma_load_3d(sL + stage * Cf::L_BYTES, &tm_l, full0 + 8u * stage, kb * kScK, 0,
-                        w.mt * kRows);
+            if (in_bounds(kb * kScK < p.vocab && w.mt * kRows < p.rows, p.status, abort_flag))
+              tma_load_3d(sL + stage * Cf::L_BYTES, &tm_l, full0 + 8u * stage, kb * kScK, 0,
+                          w.mt * kRows);
           } else {
-            mbar_arrive_expect_tx(full0 + 8u * stage, Cf::E_BYTES);  // all C slices
-            const uint32_t dst = sE + stage * Cf::E_BYTES + rank * slice * 128;
+            mbar_arrive_expect_tx(full0 + 8u * stage, Cf::E_BYTES);
+            const uint32_t dst = sE + stage * Cf::E_BYTES;
 #pragma unroll
-            for (int nb = 0; nb < kScN / 64; ++nb) {
-              if (C > 1)
-                tma_load_3d_multicast(dst + nb * (kScK * 128), &tm_e, full0 + 8u * stage,
-                                      w.nt * kScN + nb * 64, 0, kb * kScK + rank * slice, cta_mask);
-              else
-                tma_load_3d(dst + nb * (kScK * 128), &tm_e, full0 + 8u * stage,
-                            w.nt * kScN + nb * 64, 0, kb * kScK);
-            }
+            for (int nb = 0; nb < kScN / 64; ++nb)
+              // (column boxes of the last E tile past d_model are zero-filled by design)
+              if (in_bounds(kb * kScK < p.vocab && w.nt < p.n_tiles, p.status, abort_flag))
+                tma_load_3d(dst + nb * (kScK * 128), &tm_e, full0 + 8u * stage, w.nt * kScN + nb * 64, 0,
+                            kb * kScK);
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -231,7 +233,7 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
     uint32_t e_stage = 0, e_phase = 0, g = 0, ui = 0;
     bool ok = true;
     for (int64_t u = cl; ok && u < U; u += ncl, ++ui) {
-      const ScUnit w = sc_unit(p, u, C, rank);
+      const ScUnit w = sc_unit(p, u);
       // the accumulator is free once the previous unit's epilogue has read it
       if (ui > 0 &&
           !__all_sync(0xffffffffu, wait_phase(bar(Cf::B_ACC_EMPTY), (ui - 1) & 1, abort_flag, p.status))) {
@@ -255,8 +257,7 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
                             (kb == w.kb0 && kk == 0) ? 0u : 1u);
         }
         umma_commit_warp(bar(Cf::B_P_EMPTY + ps));
-        if (C > 1) umma_commit_multicast_warp(bar(Cf::B_E_EMPTY + e_stage), cta_mask);
-        else umma_commit_warp(bar(Cf::B_E_EMPTY + e_stage));
+        umma_commit_warp(bar(Cf::B_E_EMPTY + e_stage));
         if (++e_stage == kScNE) { e_stage = 0; e_phase ^= 1; }
       }
       if (!ok) break;
@@ -278,7 +279,7 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
     uint32_t l_stage = 0, l_phase = 0, g = 0, ui = 0;
     bool ok = true;
     for (int64_t u = cl; ok && u < U; u += ncl, ++ui) {
-      const ScUnit w = sc_unit(p, u, C, rank);
+      const ScUnit w = sc_unit(p, u);
       const int row = w.mt * kRows + r;
       const bool row_ok = row < p.rows;
       // rows past the end (zero-filled by TMA) get p = 2^-inf = 0
@@ -359,7 +360,8 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
             }
           }
         }
-      } else if (w.mt < p.m_tiles) {
+      } else if (w.mt < p.m_tiles &&
+                 in_bounds(w.split < p.splits && w.nt < p.n_tiles, p.status, abort_flag)) {
         // column-major partial tile: for each column the warp writes 32
         // consecutive rows (128 bytes)
         float* dst = p.part + ((static_cast<size_t>(w.split) * p.m_tiles + w.mt) * p.n_tiles + w.nt) *
@@ -383,8 +385,6 @@ sc_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUte
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // no CTA leaves while a peer may still multicast into its shared memory
-  if (C > 1) cluster_sync_all();
 }
 
 // out[r, c] = sum over splits of the partial tiles: one CTA per 128 rows x

@@ -59,33 +59,27 @@ def confidence_order(c, candidates):
     return idx[np.argsort(-np.asarray(c)[idx], kind="stable")]
 
 
-def accept(H, c, accepted_before, budget, accumulate=np.float64):
-    """New accepted flags of one canvas.  ``accumulate`` fixes the type of the
-    running entropy sum (np.float32 reproduces a sequential fp32 sum)."""
+def accept(H, c, accepted_before, budget):
+    """New accepted flags of one canvas (running entropy sum in fp64)."""
     accepted_before = np.asarray(accepted_before, dtype=bool)
     order = confidence_order(c, ~accepted_before)
     out = accepted_before.copy()
-    run = accumulate(0.0)
-    budget = accumulate(budget)
-    H = np.asarray(H)
+    run = 0.0
+    H = np.asarray(H, dtype=np.float64)
     for k, i in enumerate(order):
-        run = accumulate(run + accumulate(H[i]))
+        run += float(H[i])
         if k > 0 and run > budget:
             break
         out[i] = True
     return out
 
 
-def converge(argmax_now, argmax_prev, stable_before, H, tau, patience, step, max_steps,
-             accumulate=np.float64):
-    """(converged, stable) of one canvas after this step."""
+def converge(argmax_now, argmax_prev, stable_before, H, tau, patience, step, max_steps):
+    """(converged, stable) of one canvas after this step (mean entropy in fp64)."""
     same = bool(np.array_equal(np.asarray(argmax_now), np.asarray(argmax_prev)))
     stable = stable_before + 1 if same else 0
-    total = accumulate(0.0)
-    for h in np.asarray(H):
-        total = accumulate(total + accumulate(h))
-    mean_h = accumulate(total / accumulate(len(H)))
-    converged = (stable >= patience and mean_h < accumulate(tau)) or (step + 1 >= max_steps)
+    mean_h = float(np.sum(np.asarray(H, dtype=np.float64))) / len(H)
+    converged = (stable >= patience and mean_h < tau) or (step + 1 >= max_steps)
     return bool(converged), int(stable)
 
 

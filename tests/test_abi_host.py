@@ -96,3 +96,46 @@ def test_product_path_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", text, flags=re.M), f
                 assert "oracle/" not in text, f
+
+
+def _noalloc(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, cu_q=FAKE, ctx_len=FAKE, mode=FAKE, B=1, total_q=1 << 22,
+             total_kv=1 << 22, Hq=32, Hkv=1, D=256, window=-1, scale=0.0625, out=FAKE, lse=None,
+             stream=None)
+    a.update(kw)
+    return lib.dg_attn_forward_noalloc(a["q"], a["k"], a["v"], a["cu_q"], a["ctx_len"], a["mode"],
+                                       a["B"], a["total_q"], a["total_kv"], a["Hq"], a["Hkv"], a["D"],
+                                       a["window"], ctypes.c_float(a["scale"]), a["out"], a["lse"],
+                                       a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), binding.DG_ERR_INVALID_ARG),
+    (dict(out=FAKE + 8), binding.DG_ERR_INVALID_ARG),
+    (dict(window=-2), binding.DG_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.DG_ERR_INVALID_ARG),
+    (dict(total_kv=5), binding.DG_ERR_INVALID_ARG),
+    (dict(D=96), binding.DG_ERR_UNSUPPORTED),
+])
+def test_noalloc_checks_arguments_before_its_scratch_size(lib, kw, code):
+    """Sizes far beyond the static scratch with one bad argument: the argument
+    error is reported (as dg_attn_forward reports it), not a workspace error,
+    and nothing reaches a GPU."""
+    assert _noalloc(lib, **kw) == code
+
+
+def test_no_cluster_multicast_in_sources():
+    """Every kernel loads its operands from this GPU's memory into its own
+    shared memory: no TMA load or tcgen05 commit names a cluster multicast."""
+    for d in (os.path.join(ROOT, "dual_mode_canvas_gb300", "csrc"), os.path.join(ROOT, "include")):
+        for f in os.listdir(d):
+            text = open(os.path.join(d, f)).read()
+            assert "multicast" not in text, f
+
+
+def test_bounds_checking_build_exports_the_same_symbols():
+    dg_build.build(debug=True)
+    dbg = binding.load_library(debug=True)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    assert binding.load_library(debug=False) is not dbg

@@ -35,8 +35,8 @@ def _order_unstable_ties(c, candidates):
     return idx[np.argsort(-np.asarray(c)[idx], kind="stable")]
 
 
-def _accept_includes_overflow(H, c, before, budget, accumulate=np.float64):
-    out = _ORIG["accept"](H, c, before, budget, accumulate)
+def _accept_includes_overflow(H, c, before, budget):
+    out = _ORIG["accept"](H, c, before, budget)
     order = acc.confidence_order(c, ~np.asarray(before, dtype=bool))
     k = int((out & ~np.asarray(before, dtype=bool)).sum())
     if k < len(order):
@@ -44,7 +44,7 @@ def _accept_includes_overflow(H, c, before, budget, accumulate=np.float64):
     return out
 
 
-def _accept_no_progress(H, c, before, budget, accumulate=np.float64):
+def _accept_no_progress(H, c, before, budget):
     before = np.asarray(before, dtype=bool)
     order = acc.confidence_order(c, ~before)
     out = before.copy()
@@ -57,15 +57,15 @@ def _accept_no_progress(H, c, before, budget, accumulate=np.float64):
     return out
 
 
-def _converge_no_reset(a_now, a_prev, stable_before, H, tau, patience, step, max_steps, accumulate=np.float64):
-    cv, st = _ORIG["converge"](a_now, a_prev, stable_before, H, tau, patience, step, max_steps, accumulate)
+def _converge_no_reset(a_now, a_prev, stable_before, H, tau, patience, step, max_steps):
+    cv, st = _ORIG["converge"](a_now, a_prev, stable_before, H, tau, patience, step, max_steps)
     if st == 0:
         st = stable_before + 1
         cv = (st >= patience and float(np.mean(H)) < tau) or (step + 1 >= max_steps)
     return cv, st
 
 
-def _converge_le(a_now, a_prev, stable_before, H, tau, patience, step, max_steps, accumulate=np.float64):
+def _converge_le(a_now, a_prev, stable_before, H, tau, patience, step, max_steps):
     same = bool(np.array_equal(a_now, a_prev))
     st = stable_before + 1 if same else 0
     return bool((st >= patience and float(np.mean(H)) <= tau) or (step + 1 >= max_steps)), st

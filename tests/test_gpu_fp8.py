@@ -119,15 +119,15 @@ def test_ragged_batches(case):
         check(out, lse, b, W, f"case {case} W={W}")
 
 
-@pytest.mark.parametrize("cluster", ["1", "4"])
-def test_cluster_sizes(cluster):
-    os.environ["DG_ATTN_CLUSTER"] = cluster
+@pytest.mark.parametrize("ctas", ["1", "5"])
+def test_grid_sizes(ctas):
+    os.environ["DG_ATTN_NUM_CTAS"] = ctas
     try:
         b = wls.make_fp8_batch(wls.Workload("fp8", ((300, 256, 1), (0, 333, 0)), 8, 4, 256, -1, 74))
         out, lse = run_fp8(b, -1)
-        check(out, lse, b, -1, f"cluster {cluster}")
+        check(out, lse, b, -1, f"{ctas} CTAs")
     finally:
-        del os.environ["DG_ATTN_CLUSTER"]
+        del os.environ["DG_ATTN_NUM_CTAS"]
 
 
 def test_denoise_loop_sampled():

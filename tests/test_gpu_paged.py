@@ -4,7 +4,6 @@ seeded inputs: attention outputs within the attention bar, the cache after the
 append bit for bit, and the paged result bit-identical to the contiguous path
 on the same keys."""
 
-import os
 
 import numpy as np
 import pytest
@@ -53,12 +52,12 @@ def oracle_paged(b, window, scale):
 
 
 # (seqs, Hq, Hkv, D, page sizes, windows): page sizes below, at and above the
-# per-CTA load slice (BN / cluster size), contexts that end mid-page, a
-# sequence of one token
+# KV tile (one TMA box per page and per lane of the loader warp, up to 32
+# boxes per tile), contexts that end mid-page, a sequence of one token
 CASES = [
     (((0, 300, 0), (257, 129, 1), (1000, 256, 1), (37, 1, 0)), 8, 2, 128, (8, 16, 64, 256), (-1, 100)),
-    (((130, 77, 1), (0, 200, 0)), 2, 1, 64, (16, 128), (-1, 0, 129)),
-    (((700, 256, 1), (5, 100, 0)), 16, 2, 256, (16, 32, 1024), (-1, 129)),
+    (((130, 77, 1), (0, 200, 0)), 2, 1, 64, (8, 16, 128), (-1, 0, 129)),
+    (((700, 256, 1), (5, 100, 0)), 16, 2, 256, (8, 16, 32, 1024), (-1, 129)),
 ]
 
 
@@ -81,31 +80,22 @@ def _bits(t):
     return t.cpu().view(torch.int16).numpy()
 
 
-@pytest.mark.parametrize("cluster", ["2", "4"])
-def test_paged_equals_contiguous_bit_for_bit(cluster):
+@pytest.mark.parametrize("P", [8, 16, 64])
+def test_paged_equals_contiguous_bit_for_bit(P):
     """The same keys laid out contiguously (gathered through the page table by
-    the oracle's gather) give bit-identical outputs through dg_attn_forward,
-    with both calls in the same launch configuration (the default cluster size
-    of a paged call depends on the page size, and a different split of the
-    work changes the rounding order)."""
-    os.environ["DG_ATTN_CLUSTER"] = cluster
-    try:
-        _paged_vs_contiguous()
-    finally:
-        del os.environ["DG_ATTN_CLUSTER"]
-
-
-def _paged_vs_contiguous():
+    the oracle's gather) give bit-identical outputs through dg_attn_forward:
+    both calls split the work the same way and differ only in where each TMA
+    box of a KV tile comes from."""
     wl = wls.Workload("paged", ((300, 256, 1), (0, 333, 0), (1000, 200, 1)), 8, 4, 128, -1, 77)
-    b = wls.make_paged_batch(wl, 16, device="cuda")
+    b = wls.make_paged_batch(wl, P, device="cuda")
     d = to_dev(b)
     out_p, lse_p = run_paged(d, -1, wl.scale)
     kb, vb = _bits(d["k_cache"]), _bits(d["v_cache"])
     bt = b["block_table"].numpy()
     ks, vs = [], []
     for s, (c, n, _) in enumerate(wl.seqs):
-        ks.append(pg.gather_kv(kb, bt[s], c + n, 16))
-        vs.append(pg.gather_kv(vb, bt[s], c + n, 16))
+        ks.append(pg.gather_kv(kb, bt[s], c + n, P))
+        vs.append(pg.gather_kv(vb, bt[s], c + n, P))
     k = torch.from_numpy(np.concatenate(ks)).view(torch.bfloat16).cuda()
     v = torch.from_numpy(np.concatenate(vs)).view(torch.bfloat16).cuda()
     out_c, lse_c = binding.forward(d["q"], k, v, d["cu_q"], d["ctx_len"], d["mode"], -1, wl.scale)

@@ -118,12 +118,13 @@ def test_ragged_edge_cases(case):
         full_check(wl, batch, window=W, dev=dev, rel=EDGE_REL)
 
 
-@pytest.mark.parametrize("cluster", ["1", "2", "4", "8"])
-def test_cluster_sizes(cluster):
-    """C query tiles of one (sequence, KV head) share each K/V load through TMA
-    multicast; every cluster size gives the oracle's result, including tail
-    groups with fewer than C tiles and windowed ranges that differ per tile."""
-    os.environ["DG_ATTN_CLUSTER"] = cluster
+@pytest.mark.parametrize("ctas", ["1", "3", "37"])
+def test_grid_sizes(ctas):
+    """Persistent grids of 1, 3 and 37 CTAs cut the (tile, KV tile) units at
+    other places than the full grid: every grid gives the oracle's result,
+    with windowed ranges that differ per tile and tiles merged from several
+    CTAs' partials."""
+    os.environ["DG_ATTN_NUM_CTAS"] = ctas
     try:
         for seed, seqs, Hq, Hkv, D, windows in (
                 (41, ((300, 256, 1), (0, 333, 0), (1000, 200, 1)), 8, 4, 128, (-1, 50)),
@@ -134,7 +135,7 @@ def test_cluster_sizes(cluster):
             for W in windows:
                 full_check(wl, batch, window=W, dev=dev, rel=EDGE_REL)
     finally:
-        del os.environ["DG_ATTN_CLUSTER"]
+        del os.environ["DG_ATTN_NUM_CTAS"]
 
 
 @pytest.mark.parametrize("D", [128, 256])
@@ -202,10 +203,10 @@ def test_split_kv_matches_single_cta():
 @pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("ctas", ["152", "10"])
 def test_rotated_kv_order_matches_ascending(ctas, D):
-    """Visiting each group's KV tiles from a rotated start (the default) gives
+    """Visiting each tile's KV tiles from a rotated start (the default) gives
     the ascending-order result up to fp32 rounding, with the cut points of the
-    full grid and of a 10-CTA grid (many cuts inside each group); head_dim 256
-    runs unclustered with the softmax-side stage release, 128 in pairs."""
+    full grid and of a 10-CTA grid (many cuts inside each tile); head_dim 256
+    runs with the softmax-side stage release, 128 with the MMA warp's."""
     wl, batch = wls.random_batch(10 + D, ((3000, 256, 1), (1000, 300, 0), (500, 64, 1)), 8, 2, D, -1)
     dev = to_dev(batch)
     os.environ["DG_ATTN_NUM_CTAS"] = ctas

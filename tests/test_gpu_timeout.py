@@ -43,3 +43,30 @@ def test_expired_wait_reports_timeout_and_context_stays_usable():
                                     b["ctx_len"].numpy(), b["mode"].numpy(), -1, wl.scale)
     assert np.abs(f64(out) - ref_o).max() <= 1e-2
     assert np.abs(f64(lse) - ref_l).max() <= 1e-3
+
+
+def test_selfcond_expired_wait_reports_timeout_and_context_stays_usable():
+    """The self-conditioning GEMM's waits are bounded the same way: with
+    DG_SELFCOND_DEBUG_SKIP_E_LOAD the E loader skips one TMA load, the MMA
+    warp's wait for that stage expires, the kernel records
+    DG_ERR_DEVICE_TIMEOUT and returns; the next call is correct."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import oracle.selfcond as osc
+    binding.load_library()
+    lw = wls.LogitsWorkload("sc_timeout", (300,), 5000, 62)
+    x, _ = wls.make_logits(lw, device="cuda")
+    E = wls.make_embedding(lw.vocab, 320, 63, device="cuda")
+    assert binding.status() == binding.DG_OK
+    os.environ["DG_SELFCOND_DEBUG_SKIP_E_LOAD"] = "0"
+    try:
+        binding.self_conditioning(x, E)
+        torch.cuda.synchronize()
+    finally:
+        del os.environ["DG_SELFCOND_DEBUG_SKIP_E_LOAD"]
+    assert binding.status() == binding.DG_ERR_DEVICE_TIMEOUT
+    y = binding.self_conditioning(x, E)
+    torch.cuda.synchronize()
+    assert binding.status() == binding.DG_OK
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+    assert np.abs(f64(y) - osc.self_conditioning(f64(x), f64(E))).max() <= 1e-2
