@@ -225,7 +225,7 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
   cattr[0].val.programmaticStreamSerializationAllowed = 1;
   ccfg.attrs = cattr;
   ccfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&ccfg, combine_kernel<D>, p, num_ctas) != cudaSuccess) return DG_ERR_CUDA;
+  if (cudaLaunchKernelEx(&ccfg, combine_kernel<D>, p) != cudaSuccess) return DG_ERR_CUDA;
   return DG_OK;
 }
 

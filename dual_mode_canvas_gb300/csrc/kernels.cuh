@@ -70,6 +70,13 @@ struct TileDesc {
   int32_t causal;    // 1 causal (encoder), 0 bidirectional (denoise)
   int32_t kt_count;  // KV tiles in the range
   int32_t kt_rot;    // the KV tiles are visited from kt_first + kt_rot on, cyclically
+  // split-KV merge: the tile's KV tiles are spread over comb_n CTAs from
+  // comb_cta on (comb_n <= 1: written directly); the first of them wrote its
+  // partial to slot comb_slot0, CTA comb_cta + i (i >= 1) to slot 2 (comb_cta + i)
+  int32_t comb_cta;
+  int32_t comb_n;
+  int32_t comb_slot0;
+  int32_t pad_;
 };
 
 // KV tile (sequence-relative, units of BN keys) visited j-th for a query tile.
@@ -179,44 +186,36 @@ __device__ __forceinline__ bool in_bounds(bool ok, int* status, volatile int* ab
 }
 
 // ------------------------------------------------------------ block scan
-// In-place exclusive scan of data[0..n) (int64); data[n] receives the total.
-// Must be called by every thread of a 1024-thread block.
-__device__ void block_exclusive_scan(int64_t* data, int n) {
-  __shared__ int64_t warp_sums[32];
-  __shared__ int64_t carry;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) carry = 0;
+// Exclusive scan of one value per thread over a 1024-thread block; *total
+// receives the block's sum.  Every thread of the block must call it.
+__device__ int64_t block_scan_1024(int64_t x, int64_t* total) {
+  __shared__ int64_t warp_part[32];
+  __shared__ int64_t block_total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_part[warp] = incl;
   __syncthreads();
-  for (int base = 0; base < n; base += 1024) {
-    const int idx = base + tid;
-    int64_t x = idx < n ? data[idx] : 0;
-    int64_t incl = x;
+  if (warp == 0) {
+    const int64_t w = warp_part[lane];
+    int64_t wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+      const int64_t y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
     }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      int64_t w = warp_sums[lane];
-      int64_t wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        int64_t y = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += y;
-      }
-      warp_sums[lane] = wi - w;  // exclusive prefix of warp totals
-    }
-    __syncthreads();
-    const int64_t c0 = carry;
-    if (idx < n) data[idx] = c0 + warp_sums[warp] + incl - x;
-    __syncthreads();
-    if (tid == 1023) carry = c0 + warp_sums[31] + incl;
-    __syncthreads();
+    warp_part[lane] = wi - w;  // exclusive prefix of the warp sums
+    if (lane == 31) block_total = wi;
   }
-  if (tid == 0) data[n] = carry;
   __syncthreads();
+  const int64_t r = warp_part[warp] + incl - x;
+  *total = block_total;
+  __syncthreads();  // the shared words are reused by the next call
+  return r;
 }
 
 // ------------------------------------------------ paged cache: the append
@@ -293,7 +292,14 @@ __device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int P) {
 }
 
 // ------------------------------------------------------ work-list builder
+// Per-sequence values of the builder live in shared memory for batches of up
+// to this many sequences (larger batches read them back from the workspace).
+constexpr int kWlSmemSeqs = 1024;
+
 // CTA 0 builds the work list; with a paged cache, CTAs 1.. append the new K/V.
+// One read of the metadata, scans in registers and shared memory, one write
+// of the tile table: the attention kernel waits for this grid, so its length
+// is on every call's critical path.
 __global__ void __launch_bounds__(1024, 1)
 build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ ctx_len,
                       const uint8_t* __restrict__ mode, int B, int total_q, int total_kv, int Hkv,
@@ -307,25 +313,66 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     return;
   }
   __shared__ int bad;
+  __shared__ int32_t s_q0[kWlSmemSeqs + 1];   // cu_q
+  __shared__ int32_t s_ctx[kWlSmemSeqs];
+  __shared__ uint8_t s_mode[kWlSmemSeqs];
+  __shared__ int64_t s_toff[kWlSmemSeqs + 1];  // tiles before each sequence
+  __shared__ int64_t s_kvoff[kWlSmemSeqs];     // K/V rows before each sequence
   const int tid = threadIdx.x;
   const bool paged = pg.block_table != nullptr;
-  if (tid == 0) bad = (cu_q[0] != 0 || cu_q[B] != total_q) ? 1 : 0;
+  const bool small = B <= kWlSmemSeqs;
+  if (tid == 0) bad = 0;
   __syncthreads();
-  for (int s = tid; s < B; s += 1024) {
-    const int n = cu_q[s + 1] - cu_q[s];
-    const int c = ctx_len[s];
-    const int md = mode[s];
-    if (n < 0 || c < 0 || md > 1) atomicOr(&bad, 1);
-    const int64_t nn = n < 0 ? 0 : n;
-    const int64_t m_tiles = (nn + TT - 1) / TT;
-    ws.seq_tile_off[s] = static_cast<int64_t>(Hkv) * m_tiles;
-    ws.seq_kv_off[s] = static_cast<int64_t>(c < 0 ? 0 : c) + nn;
+  if (tid == 0 && (cu_q[0] != 0 || cu_q[B] != total_q)) atomicOr(&bad, 1);
+  // ---- sequences: tiles and K/V rows, scanned 1024 sequences at a time
+  int64_t carry_t = 0, carry_kv = 0;
+  for (int base = 0; base < B; base += 1024) {
+    const int s = base + tid;
+    int64_t nt = 0, nkv = 0;
+    if (s < B) {
+      const int q0 = cu_q[s], q1 = cu_q[s + 1], c = ctx_len[s], md = mode[s];
+      const int n = q1 - q0;
+      if (n < 0 || c < 0 || md > 1) atomicOr(&bad, 1);
+      const int64_t nn = n < 0 ? 0 : n;
+      nt = static_cast<int64_t>(Hkv) * ((nn + TT - 1) / TT);
+      nkv = static_cast<int64_t>(c < 0 ? 0 : c) + nn;
+      if (small) {
+        s_q0[s] = q0;
+        s_ctx[s] = c;
+        s_mode[s] = static_cast<uint8_t>(md);
+      }
+    }
+    int64_t sum_t, sum_kv;
+    const int64_t et = block_scan_1024(nt, &sum_t);
+    const int64_t ekv = block_scan_1024(nkv, &sum_kv);
+    if (s < B) {
+      if (small) {
+        s_toff[s] = carry_t + et;
+        s_kvoff[s] = carry_kv + ekv;
+      } else {
+        ws.seq_tile_off[s] = carry_t + et;
+        ws.seq_kv_off[s] = carry_kv + ekv;
+      }
+    }
+    carry_t += sum_t;
+    carry_kv += sum_kv;
+  }
+  if (tid == 0) {
+    if (small) {
+      s_toff[B] = carry_t;
+      s_q0[B] = total_q;
+    } else {
+      ws.seq_tile_off[B] = carry_t;
+    }
+    if (carry_t > max_tiles || (!paged && carry_kv > total_kv)) bad = 1;
   }
   __syncthreads();
+  auto q0_of = [&](int s) { return small ? s_q0[s] : cu_q[s]; };
+  auto ctx_of = [&](int s) { return small ? s_ctx[s] : ctx_len[s]; };
   if (paged && !bad) {
     // every page the attention reads: pages 0 .. ceil(L / P) - 1 of each sequence
     for (int s = 0; s < B; ++s) {
-      const int64_t L = static_cast<int64_t>(ctx_len[s]) + cu_q[s + 1] - cu_q[s];
+      const int64_t L = static_cast<int64_t>(ctx_of(s)) + q0_of(s + 1) - q0_of(s);
       const int64_t need = (L + (1 << pg.page_shift) - 1) >> pg.page_shift;
       if (need > pg.bt_stride) {
         if (tid == 0) bad = 1;
@@ -338,12 +385,6 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     }
   }
   __syncthreads();
-  block_exclusive_scan(ws.seq_tile_off, B);
-  block_exclusive_scan(ws.seq_kv_off, B);
-  if (tid == 0) {
-    if (ws.seq_tile_off[B] > max_tiles || (!paged && ws.seq_kv_off[B] > total_kv)) bad = 1;
-  }
-  __syncthreads();
   if (bad) {
     if (tid == 0) {
       ws.hdr->num_tiles = 0;
@@ -353,21 +394,25 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     }
     return;
   }
-  const int num_tiles = static_cast<int>(ws.seq_tile_off[B]);
-  for (int tile = tid; tile < num_tiles; tile += 1024) {
-    // sequence owning this tile: largest s with seq_tile_off[s] <= tile
+  // ---- tiles: thread tid owns the consecutive tiles [t_begin, t_end)
+  const int num_tiles = static_cast<int>(carry_t);
+  const int per = (num_tiles + 1023) / 1024;
+  const int t_begin = min(num_tiles, tid * per), t_end = min(num_tiles, t_begin + per);
+  auto make_tile = [&](int tile) {
+    // sequence owning this tile: largest s with tiles-before(s) <= tile
     int lo = 0, hi = B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (ws.seq_tile_off[mid] <= tile) lo = mid; else hi = mid - 1;
+      if ((small ? s_toff[mid] : ws.seq_tile_off[mid]) <= tile) lo = mid; else hi = mid - 1;
     }
     const int s = lo;
-    const int n = cu_q[s + 1] - cu_q[s];
-    const int c = ctx_len[s];
+    const int q0 = q0_of(s);
+    const int n = q0_of(s + 1) - q0;
+    const int c = ctx_of(s);
     const int L = c + n;
-    const bool causal = mode[s] == 0;
+    const bool causal = (small ? s_mode[s] : mode[s]) == 0;
     const int m_tiles = (n + TT - 1) / TT;
-    const int local = tile - static_cast<int>(ws.seq_tile_off[s]);
+    const int local = tile - static_cast<int>(small ? s_toff[s] : ws.seq_tile_off[s]);
     const int kvh = local / m_tiles;
     const int mt = local - kvh * m_tiles;
     const int t0 = mt * TT;
@@ -376,9 +421,9 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     const int kv_lo = window < 0 ? 0 : max(0, pos_first - window);
     const int kv_hi = causal ? i_max : (window < 0 ? L - 1 : min(L - 1, i_max + window));
     TileDesc td;
-    td.q_row0 = cu_q[s] + t0;
+    td.q_row0 = q0 + t0;
     td.n_tok = min(TT, n - t0);
-    td.kv_row0 = paged ? s * pg.bt_stride : static_cast<int>(ws.seq_kv_off[s]);
+    td.kv_row0 = paged ? s * pg.bt_stride : static_cast<int>(small ? s_kvoff[s] : ws.seq_kv_off[s]);
     td.pos0 = pos_first;
     td.L = L;
     td.kt_first = kv_lo / BN;
@@ -386,34 +431,49 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     td.causal = causal ? 1 : 0;
     td.kt_count = kv_hi / BN - kv_lo / BN + 1;
     td.kt_rot = 0;
-    ws.tiles[tile] = td;
-    ws.unit_begin[tile] = kSegWeight + td.kt_count;
-  }
-  __syncthreads();
-  block_exclusive_scan(ws.unit_begin, num_tiles);
-  if (tid == 0) {
-    ws.hdr->num_tiles = num_tiles;
-    ws.hdr->total_units = ws.unit_begin[num_tiles];
-    ws.hdr->error = 0;
-  }
-  if (!rotate) return;
-  // KV visiting order.  The CTAs' unit ranges are contiguous and equally
-  // long (U / P units), so the CTAs sharing one query tile start at KV-tile
-  // offsets a multiple of U / P apart.  Rotating each tile's KV tiles so that
-  // the CTA holding its first KV tile reaches that KV tile at "time" (units
-  // since the launch) equal to the KV tile's index gives every CTA of every
-  // query tile a phase that is a multiple of U / P: the query tiles of one
-  // (sequence, KV head) with the same KV range then stream the same KV tiles
-  // at about the same time, and the later readers find them in L2.  The
-  // order of the KV tiles does not change the result beyond fp32 rounding.
-  const int64_t U = ws.unit_begin[num_tiles];
+    td.comb_cta = 0;
+    td.comb_n = 0;
+    td.comb_slot0 = 0;
+    td.pad_ = 0;
+    return td;
+  };
+  // pass 1: the units of this thread's tiles, scanned over the block
+  int64_t mine = 0;
+  for (int t = t_begin; t < t_end; ++t) mine += kSegWeight + make_tile(t).kt_count;
+  int64_t U;
+  int64_t ub = block_scan_1024(mine, &U);
   const int P = active_ctas(num_ctas, U);
-  for (int tile = tid; tile < num_tiles; tile += 1024) {
-    const int64_t r0 = ws.unit_begin[tile] + kSegWeight;
-    const int64_t n = ws.unit_begin[tile + 1] - r0;
-    if (n <= 1 || P <= 1) continue;
-    const int64_t lead = r0 - cta_unit_begin(cta_of_unit(r0, U, P), U, P);  // >= 0
-    ws.tiles[tile].kt_rot = static_cast<int>(lead % n);
+  // pass 2: the finished descriptors, written once
+  for (int t = t_begin; t < t_end; ++t) {
+    TileDesc td = make_tile(t);
+    const int64_t r0 = ub + kSegWeight, n = td.kt_count;
+    // CTAs holding KV tiles of this tile, and the partial slot of the first
+    if (U > 0) {
+      const int c_lo = cta_of_unit(r0, U, P), c_hi = cta_of_unit(r0 + n - 1, U, P);
+      td.comb_cta = c_lo;
+      td.comb_n = c_hi - c_lo + 1;
+      td.comb_slot0 = cta_unit_begin(c_lo, U, P) >= ub ? 2 * c_lo : 2 * c_lo + 1;
+      // KV visiting order.  The CTAs' unit ranges are contiguous and equally
+      // long (U / P units), so the CTAs sharing one query tile start at KV-tile
+      // offsets a multiple of U / P apart.  Rotating each tile's KV tiles so
+      // that the CTA holding its first KV tile reaches that KV tile at "time"
+      // (units since the launch) equal to the KV tile's index gives every CTA
+      // of every query tile a phase that is a multiple of U / P: the query
+      // tiles of one (sequence, KV head) with the same KV range then stream the
+      // same KV tiles at about the same time, and the later readers find them
+      // in L2.  The order of the KV tiles does not change the result beyond
+      // fp32 rounding.
+      if (rotate && n > 1 && P > 1) td.kt_rot = static_cast<int>((r0 - cta_unit_begin(c_lo, U, P)) % n);
+    }
+    ws.tiles[t] = td;
+    ws.unit_begin[t] = ub;
+    ub += kSegWeight + n;
+  }
+  if (tid == 0) {
+    ws.unit_begin[num_tiles] = U;
+    ws.hdr->num_tiles = num_tiles;
+    ws.hdr->total_units = U;
+    ws.hdr->error = 0;
   }
 }
 
@@ -572,11 +632,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
            const FwdParams p) {
   using Cf = FwdCfg<D, BN, NK, NV, F8>;
   using E = Elem<F8>;
-  // launched as a programmatic dependent of the work-list grid: nothing it
-  // wrote is read before that grid has finished.  The split-KV merge is this
-  // grid's own dependent: it may launch at once and become resident as CTAs
-  // of this grid exit; it waits for this grid before reading the partials.
-  griddep_wait();
+  // launched as a programmatic dependent of the work-list grid: the prologue
+  // (barriers, TMEM, descriptor prefetch) overlaps that grid, and nothing it
+  // wrote is read before it has finished.  The split-KV merge is this grid's
+  // own dependent: it may launch at once and become resident as CTAs of this
+  // grid exit; it waits for this grid before reading the partials.
   griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -586,15 +646,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const WorkHeader* hdr = p.ws.hdr;
-  const int num_tiles = hdr->num_tiles;
-  const int64_t U = hdr->total_units;
-  const int cta = static_cast<int>(blockIdx.x);
-  if (num_tiles <= 0 || U <= 0) return;  // uniform over the grid
-  const int P = active_ctas(static_cast<int>(gridDim.x), U);
-  if (cta >= P) return;  // uniform over the CTA
-  const int64_t u_beg = cta_unit_begin(cta, U, P);
-  const int64_t u_end = cta_unit_begin(cta + 1, U, P);
   // Soft release (64-key tiles): a softmax thread frees the K and V stages
   // with an arrive once it has seen S(g), so the loaders wait on K_EMPTY /
   // V_EMPTY; measured 1.5% faster there than freeing them through the MMA
@@ -648,6 +699,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   // all 512 columns of all 128 lanes: the column offsets below are compile-time
   // constants within that range (checked by FwdCfg's static_asserts)
   in_bounds(tmem == 0u, p.status, abort_flag);
+
+  griddep_wait();
+  const WorkHeader* hdr = p.ws.hdr;
+  const int num_tiles = hdr->num_tiles;
+  const int64_t U = hdr->total_units;
+  const int cta = static_cast<int>(blockIdx.x);
+  const int P = U > 0 ? active_ctas(static_cast<int>(gridDim.x), U) : 1;
+  // a CTA without work (no tiles, or more CTAs than units) walks an empty
+  // range: every role finds nothing to do and the CTA frees its TMEM
+  const bool active = num_tiles > 0 && U > 0 && cta < P;
+  const int64_t u_beg = active ? cta_unit_begin(cta, U, P) : 0;
+  const int64_t u_end = active ? cta_unit_begin(cta + 1, U, P) : 0;
 
   SegIter it{p.ws.unit_begin, num_tiles, u_beg, u_end, cta, true};
   const int G = p.G, TT = p.TT;
@@ -1063,33 +1126,31 @@ constexpr int kCombineWarps = 8;
 
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
-combine_kernel(const FwdParams p, int num_ctas) {
-  const WorkHeader* hdr = p.ws.hdr;
+combine_kernel(const FwdParams p) {
   const int tile = blockIdx.x;
-  if (tile >= hdr->num_tiles) return;
-  const int64_t U = hdr->total_units;
-  const int P = active_ctas(num_ctas, U);
-  const int64_t T0 = p.ws.unit_begin[tile], T1 = p.ws.unit_begin[tile + 1];
-  const int c_lo = cta_of_unit(T0 + kSegWeight, U, P);  // CTAs holding KV tiles of the tile
-  const int c_hi = cta_of_unit(T1 - 1, U, P);
-  if (c_lo == c_hi) return;  // written directly by one CTA
-  const TileDesc td = p.ws.tiles[tile];
   const int G = p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * kCombineWarps + warp;
   if (r >= G * p.TT) return;
   const int t = r / G, gi = r - t * G;
-  if (t >= td.n_tok) return;
-  const int nc = c_hi - c_lo + 1;
-  // a CTA's first segment uses slot 2c, its later one 2c + 1
-  auto slot_of = [&](int c) { return cta_unit_begin(c, U, P) >= T0 ? 2 * c : 2 * c + 1; };
-  // the partials are written by the attention grid, this grid's predecessor
+  // the tile table and the partials are written by the preceding grids
   griddep_wait();
+  // both loads issued together (the descriptor of a tile past num_tiles is
+  // stale but lies inside the workspace and is not used)
+  const int num_tiles = p.ws.hdr->num_tiles;
+  const TileDesc td = p.ws.tiles[tile];
+  if (tile >= num_tiles || td.comb_n <= 1) return;  // no tile, or written directly by one CTA
+  if (t >= td.n_tok) return;
+  const int nc = td.comb_n;
+  // partial slot of contributor i: the first CTA's is recorded, the others
+  // hold the tile in their first segment
+  auto slot_of = [&](int i) { return i == 0 ? td.comb_slot0 : 2 * (td.comb_cta + i); };
   constexpr int E = D / 32;  // columns per lane
   const int orow = td.q_row0 + t;
   const int h = td.kvh * G + gi;
   // every partial slot this row reads and the row it writes
-  if (!in_bounds(orow >= 0 && orow < p.total_q && h < p.Hq && c_lo >= 0 && slot_of(c_hi) < p.num_slots,
+  if (!in_bounds(orow >= 0 && orow < p.total_q && h < p.Hq && td.comb_slot0 >= 0 &&
+                     td.comb_slot0 < p.num_slots && slot_of(nc - 1) < p.num_slots,
                  p.status, nullptr))
     return;
   __nv_bfloat16* dst = p.out + (static_cast<size_t>(orow) * p.Hq + h) * D;
@@ -1100,7 +1161,7 @@ combine_kernel(const FwdParams p, int num_ctas) {
     float acc4[4][E];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int sl = slot_of(c_lo + min(u, nc - 1));
+      const int sl = slot_of(min(u, nc - 1));
       lw[u] = u < nc ? p.ws.part_lse[static_cast<size_t>(sl) * kRows + r] : -INFINITY;
       const float* src = p.ws.part_o + (static_cast<size_t>(sl) * kRows + r) * D;
       if constexpr (E % 4 == 0) {
@@ -1148,7 +1209,7 @@ combine_kernel(const FwdParams p, int num_ctas) {
   // every contributor's LSE at once (lane i holds contributors i, i + 32, ...)
   float M = -INFINITY;
   for (int i = lane; i < nc; i += 32)
-    M = fmaxf(M, p.ws.part_lse[static_cast<size_t>(slot_of(c_lo + i)) * kRows + r]);
+    M = fmaxf(M, p.ws.part_lse[static_cast<size_t>(slot_of(i)) * kRows + r]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[E];
@@ -1158,7 +1219,7 @@ combine_kernel(const FwdParams p, int num_ctas) {
   for (int i0 = 0; i0 < nc; i0 += 32) {
     // lane j: weight and slot of contributor i0 + j
     const int cj = i0 + lane;
-    const int sj = cj < nc ? slot_of(c_lo + cj) : 0;
+    const int sj = cj < nc ? slot_of(cj) : 0;
     const float lj = cj < nc ? p.ws.part_lse[static_cast<size_t>(sj) * kRows + r] : -INFINITY;
     const float wj = lj == -INFINITY ? 0.f : __expf(lj - M);
     float ws = wj;
