@@ -847,11 +847,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             tc_fence_after();
             const uint32_t d_s = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
             const uint32_t k_base = sK + k_stage * Cf::KV_BYTES;
+            // one batch of four K steps per 128-byte column block of K: A
+            // advances 8 TMEM columns, B 32 bytes within the swizzle atom
 #pragma unroll
-            for (int kk = 0; kk < D / E::KSTEP; ++kk) {
-              const uint64_t b = smem_desc_sw128(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-              if constexpr (F8) umma_e4m3_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
-              else umma_bf16_ts_warp(d_s, tmem + Cf::TM_Q + kk * 8, b, idesc_qk, kk > 0 ? 1u : 0u);
+            for (int kb = 0; kb < Cf::NKB; ++kb) {
+              const uint64_t b = smem_desc_sw128(k_base + kb * (BN * 128), 16, 1024);
+              umma_ts_batch_warp<F8, 4>(d_s, tmem + Cf::TM_Q + kb * 32, b, idesc_qk, kb > 0 ? 1u : 0u, 8u, 2ull);
             }
             umma_commit_warp(bar(Cf::B_S_FULL + k_stage));
             if (++k_stage == NK) { k_stage = 0; k_phase ^= 1; }
@@ -872,13 +873,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             tc_fence_after();
             const uint32_t p_tm = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
             const uint32_t v_base = sV + v_stage * Cf::KV_BYTES;
+            // batches of (up to) four K steps: A advances 8 TMEM columns, B one
+            // K step of V rows (KSTEP rows of 128 bytes)
+            constexpr int kPvSteps = BN / E::KSTEP;
+            constexpr int kPvBatch = kPvSteps % 4 == 0 ? 4 : 2;
+            static_assert(kPvSteps % kPvBatch == 0, "P.V steps in batches of 2 or 4");
 #pragma unroll
-            for (int kk = 0; kk < BN / E::KSTEP; ++kk) {
-              const uint64_t b = smem_desc_sw128(v_base + kk * (E::KSTEP * 128), BN * 128, 1024);
-              if constexpr (F8)
-                umma_e4m3_ts_warp(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
-              else
-                umma_bf16_ts_warp(tmem + Cf::TM_O, p_tm + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+            for (int kb = 0; kb < kPvSteps / kPvBatch; ++kb) {
+              const uint64_t b = smem_desc_sw128(v_base + kb * kPvBatch * (E::KSTEP * 128), BN * 128, 1024);
+              umma_ts_batch_warp<F8, kPvBatch>(tmem + Cf::TM_O, p_tm + kb * kPvBatch * 8, b, idesc_pv,
+                                               (first && kb == 0) ? 0u : 1u, 8u,
+                                               static_cast<uint64_t>(E::KSTEP * 128 / 16));
             }
             umma_commit_warp(bar(Cf::B_O_DONE + v_stage));
             if (++v_stage == NV) { v_stage = 0; v_phase ^= 1; }

@@ -153,6 +153,53 @@ __device__ __forceinline__ void umma_e4m3_ts_warp(uint32_t d_tmem, uint32_t a_tm
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// N (2 or 4) MMAs of one batch in one asm block: one elect.sync for all of
+// them; the k-th (k = 0 .. N-1) reads A at a_tmem + k * a_step and B through
+// b_desc + k * b_step (descriptor units: 16 bytes of start address).  The
+// first one overwrites D when accumulate == 0, the others always accumulate.
+#define DG_UMMA_X2(KIND)                                                                       \
+  "{\n\t.reg .pred e, p, t;\n\t.reg .b64 b1;\n\t.reg .b32 a1;\n\t"                              \
+  "elect.sync _|e, 0xffffffff;\n\t"                                                           \
+  "setp.ne.b32 p, %4, 0;\n\t"                                                                 \
+  "setp.eq.b32 t, %4, %4;\n\t"                                                                \
+  "add.s64 b1, %2, %6;\n\t"                                                                   \
+  "add.u32 a1, %1, %5;\n\t"                                                                   \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [%1], %2, %3, p;\n\t"                    \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [a1], b1, %3, t;\n\t}"
+#define DG_UMMA_X4(KIND)                                                                       \
+  "{\n\t.reg .pred e, p, t;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 a1, a2, a3;\n\t"              \
+  "elect.sync _|e, 0xffffffff;\n\t"                                                           \
+  "setp.ne.b32 p, %4, 0;\n\t"                                                                 \
+  "setp.eq.b32 t, %4, %4;\n\t"                                                                \
+  "add.s64 b1, %2, %6;\n\tadd.s64 b2, b1, %6;\n\tadd.s64 b3, b2, %6;\n\t"                     \
+  "add.u32 a1, %1, %5;\n\tadd.u32 a2, a1, %5;\n\tadd.u32 a3, a2, %5;\n\t"                     \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [%1], %2, %3, p;\n\t"                    \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [a1], b1, %3, t;\n\t"                    \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [a2], b2, %3, t;\n\t"                    \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [a3], b3, %3, t;\n\t}"
+
+template <bool F8, int N>
+__device__ __forceinline__ void umma_ts_batch_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate, uint32_t a_step,
+                                                   uint64_t b_step) {
+  static_assert(N == 2 || N == 4, "batches of 2 or 4 MMAs");
+  if constexpr (N == 4 && F8) {
+    asm volatile(DG_UMMA_X4("f8f6f4") ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                 "r"(a_step), "l"(b_step) : "memory");
+  } else if constexpr (N == 4) {
+    asm volatile(DG_UMMA_X4("f16") ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                 "r"(a_step), "l"(b_step) : "memory");
+  } else if constexpr (F8) {
+    asm volatile(DG_UMMA_X2("f8f6f4") ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                 "r"(a_step), "l"(b_step) : "memory");
+  } else {
+    asm volatile(DG_UMMA_X2("f16") ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                 "r"(a_step), "l"(b_step) : "memory");
+  }
+}
+#undef DG_UMMA_X2
+#undef DG_UMMA_X4
+
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
