@@ -57,12 +57,16 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // BN columns and Q) and K-ring / V-ring stages (shared memory holds only the
 // rings, up to 224 KB).
 // e4m3 tiles are half the bytes: the same rings hold more stages.
+// NS S/P buffers: head_dim 64 has TMEM room for three (64 + 3 x 128 + 32
+// columns), so QK^T runs two tiles ahead of P.V; the others keep two.
+// (96-key tiles with three buffers at head_dim 128 were measured slower than
+// 128-key tiles with two: max mix 0.902 vs 0.840 ms per call.)
 template <int D, bool F8 = false> struct Shape;
-template <> struct Shape<64> { static constexpr int BN = 128, NK = 6, NV = 6; };
-template <> struct Shape<128> { static constexpr int BN = 128, NK = 4, NV = 3; };
-template <> struct Shape<256> { static constexpr int BN = 64, NK = 4, NV = 3; };
-template <> struct Shape<128, true> { static constexpr int BN = 128, NK = 6, NV = 6; };
-template <> struct Shape<256, true> { static constexpr int BN = 64, NK = 6, NV = 6; };
+template <> struct Shape<64> { static constexpr int BN = 128, NK = 6, NV = 6, NS = 3; };
+template <> struct Shape<128> { static constexpr int BN = 128, NK = 4, NV = 3, NS = 2; };
+template <> struct Shape<256> { static constexpr int BN = 64, NK = 4, NV = 3, NS = 2; };
+template <> struct Shape<128, true> { static constexpr int BN = 128, NK = 6, NV = 6, NS = 2; };
+template <> struct Shape<256, true> { static constexpr int BN = 64, NK = 6, NV = 6, NS = 2; };
 
 int kv_tile_rows(int D, bool f8 = false) {
   if (f8) return D == 128 ? Shape<128, true>::BN : Shape<256, true>::BN;
@@ -72,8 +76,8 @@ int kv_tile_rows(int D, bool f8 = false) {
 template <int D, bool F8 = false>
 cudaError_t set_kernel_attrs() {
   using S = Shape<D, F8>;
-  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8>;
-  return cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV, F8>,
+  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8, S::NS>;
+  return cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV, F8, S::NS>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
 }
 
@@ -198,7 +202,7 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
                    const FwdParams& p, int num_ctas, int max_tiles, cudaStream_t stream,
                    cudaEvent_t ev_begin, cudaEvent_t ev_end) {
   using S = Shape<D, F8>;
-  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8>;
+  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8, S::NS>;
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DG_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
@@ -211,7 +215,7 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV, F8>, mk, mv, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV, F8, S::NS>, mk, mv, p) != cudaSuccess)
     return DG_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return DG_ERR_CUDA;
   // the merge is a programmatic dependent of the attention grid (it waits
@@ -304,7 +308,12 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   const int BN = kv_tile_rows(head_dim, f8);
   CUtensorMap mk, mv;
   // K/V tiles of BN rows; from a paged cache in boxes of at most one page
-  const int box = pg ? std::min(1 << pg->page_shift, BN) : BN;
+  // that divide the tile (pages and tiles start on multiples of the box)
+  int box = BN;
+  if (pg) {
+    box = 1;
+    while (box * 2 <= (1 << pg->page_shift) && BN % (box * 2) == 0) box *= 2;
+  }
   const void* kmap = pg ? pg->k_cache : k;
   const void* vmap = pg ? pg->v_cache : v;
   const int map_rows = pg ? (pg->num_pages << pg->page_shift) : total_kv;

@@ -595,7 +595,7 @@ struct Elem {
 };
 
 // Shared memory holds only the K and V rings; Q, S, P and O live in TMEM.
-template <int D, int BN, int NK, int NV, bool F8 = false>
+template <int D, int BN, int NK, int NV, bool F8 = false, int NS = 2>
 struct FwdCfg {
   using E = Elem<F8>;
   static constexpr int NKB = D * E::SIZE / 128;      // 128-byte column blocks of head_dim
@@ -610,27 +610,30 @@ struct FwdCfg {
   // (with soft release, K_EMPTY / V_EMPTY free the stages instead)
   static constexpr int B_Q_FULL = 0, B_K_FULL = 1, B_V_FULL = 1 + NK,
                        B_S_FULL = 1 + NK + NV, B_P_FULL = B_S_FULL + NK,
-                       B_O_DONE = B_P_FULL + 2, B_K_EMPTY = B_O_DONE + NV, B_V_EMPTY = B_K_EMPTY + NK,
+                       B_O_DONE = B_P_FULL + NS, B_K_EMPTY = B_O_DONE + NV, B_V_EMPTY = B_K_EMPTY + NK,
                        B_O_FREE = B_V_EMPTY + NV,
                        B_DRAIN = B_O_FREE + 1, NUM_BARS = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
-  // TMEM columns: O (fp32, D), two S buffers (fp32, BN; P overwrites the first
-  // BN / PER_WORD columns, packed), Q (packed, D / PER_WORD)
-  static constexpr uint32_t TM_O = 0, TM_S0 = D, TM_S1 = D + BN, TM_Q = D + 2 * BN;
+  // TMEM columns: O (fp32, D), NS S buffers (fp32, BN; P overwrites the first
+  // BN / PER_WORD columns, packed), Q (packed, D / PER_WORD).  Tile g uses S
+  // buffer g % NS; the MMA warp issues QK^T NS - 1 tiles ahead of P.V.
+  static constexpr uint32_t TM_O = 0, TM_Q = D + NS * BN;
+  static __device__ __forceinline__ uint32_t tm_s(uint32_t g) { return D + (g % NS) * BN; }
   static_assert(D % 64 == 0 && D >= 64 && D <= 256, "head_dim");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "kv tile");
+  static_assert(NS == 2 || NS == 3, "two or three S/P buffers");
   static_assert(NKB >= 1, "head_dim of at least one 128-byte block");
-  static_assert(D + 2 * BN + D / E::PER_WORD <= static_cast<int>(kTmemCols), "TMEM budget");
+  static_assert(D + NS * BN + D / E::PER_WORD <= static_cast<int>(kTmemCols), "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <int D, int BN, int NK, int NV, bool F8 = false>
+template <int D, int BN, int NK, int NV, bool F8 = false, int NS = 2>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const FwdParams p) {
-  using Cf = FwdCfg<D, BN, NK, NV, F8>;
+  using Cf = FwdCfg<D, BN, NK, NV, F8, NS>;
   using E = Elem<F8>;
   // launched as a programmatic dependent of the work-list grid: the prologue
   // (barriers, TMEM, descriptor prefetch) overlaps that grid, and nothing it
@@ -649,8 +652,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   // Soft release (64-key tiles): a softmax thread frees the K and V stages
   // with an arrive once it has seen S(g), so the loaders wait on K_EMPTY /
   // V_EMPTY; measured 1.5% faster there than freeing them through the MMA
-  // warp's S_FULL / O_DONE commits, which the 128-key tiles use.
+  // warp's S_FULL / O_DONE commits, which the larger tiles use.  (It relies
+  // on P.V running one tile behind QK^T: two S/P buffers.)
   constexpr bool soft_release = (BN == 64);
+  static_assert(!soft_release || NS == 2, "soft release with two S/P buffers");
+  constexpr int LA = NS - 1;  // P.V of tile g is issued after QK^T of tile g + LA
 
   const uint32_t sK = sbase + Cf::OFF_K;
   const uint32_t sV = sbase + Cf::OFF_V;
@@ -675,9 +681,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       mbar_init(bar(Cf::B_O_DONE + s), 1);
       mbar_init(bar(Cf::B_V_EMPTY + s), 1);
     }
-    // one P_FULL per S/P buffer in TMEM: tile g uses index g & 1
-    mbar_init(bar(Cf::B_P_FULL + 0), kRows);
-    mbar_init(bar(Cf::B_P_FULL + 1), kRows);
+    // one P_FULL per S/P buffer in TMEM: tile g uses index g % NS
+    for (int s = 0; s < NS; ++s) mbar_init(bar(Cf::B_P_FULL + s), kRows);
     mbar_init(bar(Cf::B_O_FREE), kRows);
     mbar_init(bar(Cf::B_DRAIN), 1);
     *abort_flag = 0;
@@ -812,10 +817,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    // per KV tile g: S[g&1] = Q K^T (A = Q from TMEM), then, one tile later,
-    // O += P V with P read from TMEM where it overwrote S[g&1].  MMAs of one
-    // thread execute in issue order, so QK(g+2) may reuse the buffer as soon
-    // as PV(g) has been issued.  The whole warp runs this loop with identical
+    // per KV tile g: S[g % NS] = Q K^T (A = Q from TMEM), then, LA = NS - 1
+    // tiles later, O += P V with P read from TMEM where it overwrote
+    // S[g % NS].  MMAs of one thread execute in issue order, so QK(g + NS)
+    // may reuse the buffer as soon as PV(g) has been issued.  The whole warp runs this loop with identical
     // (warp-uniform) operands and one elected lane issues each tcgen05 op:
     // issuing from a single divergent lane cost ~100 clocks per MMA.
     //
@@ -838,14 +843,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_Q_FULL), seg_i & 1, abort_flag, p.status))) { ok = false; break; }
         tc_fence_after();
         const int n = sg.j1 - sg.j0;
-        for (int jj = 0; jj <= n && ok; ++jj) {
+        for (int jj = 0; jj < n + LA && ok; ++jj) {
           if (jj < n) {
             const uint32_t g = gj + jj;
             if (!k_ready &&
                 !__all_sync(0xffffffffu, wait_phase(bar(Cf::B_K_FULL + k_stage), k_phase, abort_flag, p.status))) { ok = false; break; }
             k_ready = false;
             tc_fence_after();
-            const uint32_t d_s = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
+            const uint32_t d_s = tmem + Cf::tm_s(g);
             const uint32_t k_base = sK + k_stage * Cf::KV_BYTES;
             // one batch of four K steps per 128-byte column block of K: A
             // advances 8 TMEM columns, B 32 bytes within the swizzle atom
@@ -857,21 +862,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             umma_commit_warp(bar(Cf::B_S_FULL + k_stage));
             if (++k_stage == NK) { k_stage = 0; k_phase ^= 1; }
           }
-          if (jj >= 1) {
-            const uint32_t g = gj + jj - 1;
-            const bool first = (jj == 1);
+          if (jj >= LA) {
+            const uint32_t g = gj + jj - LA;
+            const bool first = (jj == LA);
             if (first && seg_i > 0 &&
                 !__all_sync(0xffffffffu, wait_phase(bar(Cf::B_O_FREE), (seg_i - 1) & 1, abort_flag, p.status))) { ok = false; break; }
             // k_stage / k_phase already name the next QK's stage (this segment
             // or the next); at the end of the work that phase never completes
             // and the probe just reads false
             bool kr = k_ready;
-            const bool w = wait_pv_probe_k(bar(Cf::B_P_FULL + (g & 1)), (g >> 1) & 1, bar(Cf::B_V_FULL + v_stage),
+            const bool w = wait_pv_probe_k(bar(Cf::B_P_FULL + g % NS), (g / NS) & 1, bar(Cf::B_V_FULL + v_stage),
                                            v_phase, bar(Cf::B_K_FULL + k_stage), k_phase, kr, abort_flag, p.status);
             k_ready = __all_sync(0xffffffffu, kr);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t p_tm = tmem + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
+            const uint32_t p_tm = tmem + Cf::tm_s(g);
             const uint32_t v_base = sV + v_stage * Cf::KV_BYTES;
             // batches of (up to) four K steps: A advances 8 TMEM columns, B one
             // K step of V rows (KSTEP rows of 128 bytes)
@@ -975,7 +980,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         }
         tc_fence_after();
         uint32_t sr[BN];
-        const uint32_t s_addr = lane_base + ((g & 1) ? Cf::TM_S1 : Cf::TM_S0);
+        const uint32_t s_addr = lane_base + Cf::tm_s(g);
         if constexpr (BN == 64) tmem_ld64(s_addr, sr);
         else tmem_ld128(s_addr, sr);
         float s[BN];
@@ -1047,7 +1052,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         // P row (bf16 pairs) over the first BN/2 columns of this S buffer
         store_packed_p(s_addr, pk);
         tc_fence_before();
-        mbar_arrive(bar(Cf::B_P_FULL + (g & 1)));
+        mbar_arrive(bar(Cf::B_P_FULL + g % NS));
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
