@@ -76,6 +76,23 @@ def test_paged_matches_oracle(case):
             np.testing.assert_array_equal(f64(d["v_cache"]), va)
 
 
+@pytest.mark.parametrize("name", ["mixed_full", "mixed_w512"])
+@pytest.mark.parametrize("P", [16, 64])
+def test_configured_mixed_batches_at_the_plain_bar(name, P):
+    """The configured mixed batches (causal prefills and canvases over cached
+    contexts, GQA 16/8, head_dim 128, full and W=512 layers) through the paged
+    cache, every element against the oracle at the stated bar (max 1e-2, mean
+    1e-3, LSE 1e-3): the plain bar, not the edge-case one."""
+    wl = wls.WORKLOADS[name]
+    b = wls.make_paged_batch(wl, P, device="cuda")
+    d = to_dev(b)
+    out, lse = run_paged(d, wl.window, wl.scale)
+    ro, rl, ka, va = oracle_paged(b, wl.window, wl.scale)
+    check(f64(out), f64(lse), ro, rl, f"{name} P={P}")
+    np.testing.assert_array_equal(f64(d["k_cache"]), ka)
+    np.testing.assert_array_equal(f64(d["v_cache"]), va)
+
+
 def _bits(t):
     return t.cpu().view(torch.int16).numpy()
 
