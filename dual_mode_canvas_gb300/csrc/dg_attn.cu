@@ -53,20 +53,26 @@ struct NvtxRange {
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// Per-head_dim kernel shapes: KV tile rows (TMEM holds O, two S/P buffers of
-// BN columns and Q) and K-ring / V-ring stages (shared memory holds only the
-// rings, up to 224 KB).
-// e4m3 tiles are half the bytes: the same rings hold more stages.
-// NS S/P buffers: head_dim 64 has TMEM room for three (64 + 3 x 128 + 32
-// columns), so QK^T runs two tiles ahead of P.V; the others keep two.
-// (96-key tiles with three buffers at head_dim 128 were measured slower than
-// 128-key tiles with two: max mix 0.902 vs 0.840 ms per call.)
+// Per-head_dim kernel shapes: KV tile rows BN, K-ring and V-ring stages
+// (shared memory holds the rings, up to 224 KB, and with QS the query tile),
+// S/P buffers NS in TMEM (O, NS buffers of BN columns and, without QS, Q).
+// - head_dim 64 has TMEM room for three buffers (64 + 3 x 128 + 32 columns),
+//   so QK^T runs two tiles ahead of P.V.
+// - bf16 head_dim 128 / 256 keep two: 96-key tiles with three buffers were
+//   slower at head_dim 128 (max mix 0.902 vs 0.840 ms per call), and so was the
+//   query tile in shared memory with three 128-key buffers (0.827 vs 0.820 ms;
+//   at head_dim 256 the 64 KB query tile leaves five ring stages: denoise loop
+//   0.198 vs 0.172 ms).
+// - e4m3 tiles are half the bytes, so the same rings hold more stages, and
+//   three buffers pay: head_dim 256 has TMEM room for them (256 + 3 x 64 + 64
+//   columns; denoise loop 0.137 vs 0.145 ms), head_dim 128 moves its query tile
+//   to shared memory for them (max mix 0.691 vs 0.698 ms).
 template <int D, bool F8 = false> struct Shape;
-template <> struct Shape<64> { static constexpr int BN = 128, NK = 6, NV = 6, NS = 3; };
-template <> struct Shape<128> { static constexpr int BN = 128, NK = 4, NV = 3, NS = 2; };
-template <> struct Shape<256> { static constexpr int BN = 64, NK = 4, NV = 3, NS = 2; };
-template <> struct Shape<128, true> { static constexpr int BN = 128, NK = 6, NV = 6, NS = 2; };
-template <> struct Shape<256, true> { static constexpr int BN = 64, NK = 6, NV = 6, NS = 2; };
+template <> struct Shape<64> { static constexpr int BN = 128, NK = 6, NV = 6, NS = 3; static constexpr bool QS = false; };
+template <> struct Shape<128> { static constexpr int BN = 128, NK = 4, NV = 3, NS = 2; static constexpr bool QS = false; };
+template <> struct Shape<256> { static constexpr int BN = 64, NK = 4, NV = 3, NS = 2; static constexpr bool QS = false; };
+template <> struct Shape<128, true> { static constexpr int BN = 128, NK = 6, NV = 6, NS = 3; static constexpr bool QS = true; };
+template <> struct Shape<256, true> { static constexpr int BN = 64, NK = 6, NV = 6, NS = 3; static constexpr bool QS = false; };
 
 int kv_tile_rows(int D, bool f8 = false) {
   if (f8) return D == 128 ? Shape<128, true>::BN : Shape<256, true>::BN;
@@ -76,8 +82,8 @@ int kv_tile_rows(int D, bool f8 = false) {
 template <int D, bool F8 = false>
 cudaError_t set_kernel_attrs() {
   using S = Shape<D, F8>;
-  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8, S::NS>;
-  return cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV, F8, S::NS>,
+  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8, S::NS, S::QS>;
+  return cudaFuncSetAttribute(fwd_kernel<D, S::BN, S::NK, S::NV, F8, S::NS, S::QS>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
 }
 
@@ -202,7 +208,7 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
                    const FwdParams& p, int num_ctas, int max_tiles, cudaStream_t stream,
                    cudaEvent_t ev_begin, cudaEvent_t ev_end) {
   using S = Shape<D, F8>;
-  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8, S::NS>;
+  using C = FwdCfg<D, S::BN, S::NK, S::NV, F8, S::NS, S::QS>;
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DG_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
@@ -215,7 +221,7 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV, F8, S::NS>, mk, mv, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, fwd_kernel<D, S::BN, S::NK, S::NV, F8, S::NS, S::QS>, mk, mv, p) != cudaSuccess)
     return DG_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return DG_ERR_CUDA;
   // the merge is a programmatic dependent of the attention grid (it waits

@@ -550,8 +550,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the P and V of one PV together and, in the same rounds, tests the
-// K stage of the next QK^T.  Each mbarrier test costs the MMA warp ~130 clocks
-// of latency; the three are independent, so one round costs about one test.
+// K stage of the next QK^T (each test is its own block: measured faster than
+// issuing the three tests of a round in one block, 413 vs 769 clocks from the
+// last P arrival to the MMA warp seeing it on the max mix).
 __device__ __forceinline__ bool wait_pv_probe_k(uint32_t pbar, uint32_t pparity, uint32_t vbar,
                                                 uint32_t vparity, uint32_t kbar, uint32_t kparity,
                                                 bool& k_ready, volatile int* abort_flag, int* status) {
@@ -594,15 +595,21 @@ struct Elem {
   static constexpr float LAZY = F8 ? 3.f : 8.f;
 };
 
-// Shared memory holds only the K and V rings; Q, S, P and O live in TMEM.
-template <int D, int BN, int NK, int NV, bool F8 = false, int NS = 2>
+// Shared memory holds the K and V rings and, with QS, the query tile; S, P
+// and O (and Q without QS) live in TMEM.
+template <int D, int BN, int NK, int NV, bool F8 = false, int NS = 2, bool QS = false>
 struct FwdCfg {
   using E = Elem<F8>;
   static constexpr int NKB = D * E::SIZE / 128;      // 128-byte column blocks of head_dim
   static constexpr int KV_BYTES = BN * D * E::SIZE;  // one K (or V) tile
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
+  // QS: the query tile in shared memory, K-major with the 128-byte swizzle
+  // (NKB blocks of 128 rows x 128 bytes), read by QK^T in SS form.  That frees
+  // Q's TMEM columns for a third S/P buffer.
+  static constexpr int OFF_Q = OFF_V + NV * KV_BYTES;
+  static constexpr int Q_BYTES = QS ? kRows * D * E::SIZE : 0;
+  static constexpr int OFF_BAR = OFF_Q + Q_BYTES;
   // barriers
   // S_FULL[s]: QK^T of the tile in K stage s is done (which also frees that
   // K stage); O_DONE[s]: likewise P.V of the tile in V stage s (which frees
@@ -617,23 +624,33 @@ struct FwdCfg {
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
   // TMEM columns: O (fp32, D), NS S buffers (fp32, BN; P overwrites the first
-  // BN / PER_WORD columns, packed), Q (packed, D / PER_WORD).  Tile g uses S
-  // buffer g % NS; the MMA warp issues QK^T NS - 1 tiles ahead of P.V.
+  // BN / PER_WORD columns, packed), Q (packed, D / PER_WORD; not with QS).
+  // Tile g uses S buffer g % NS; the MMA warp issues QK^T NS - 1 tiles ahead
+  // of P.V.
   static constexpr uint32_t TM_O = 0, TM_Q = D + NS * BN;
   static __device__ __forceinline__ uint32_t tm_s(uint32_t g) { return D + (g % NS) * BN; }
   static_assert(D % 64 == 0 && D >= 64 && D <= 256, "head_dim");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "kv tile");
   static_assert(NS == 2 || NS == 3, "two or three S/P buffers");
   static_assert(NKB >= 1, "head_dim of at least one 128-byte block");
-  static_assert(D + NS * BN + D / E::PER_WORD <= static_cast<int>(kTmemCols), "TMEM budget");
+  // Barrier reuse: S_FULL[g % NK] and O_DONE[g % NV] serve every NK-th (NV-th)
+  // tile; a parity wait is sound while the barrier is at most one phase away
+  // from the awaited one.  QK^T(g + NK) waits for P(g + NK - NS), so the
+  // softmax has seen S(g) before S_FULL moves on when NK >= NS; the rescale
+  // wait for PV(g - 1) at tile g needs PV(g - 1 - NV) done, which S(g) seen
+  // implies (PV(g - NS) was issued before QK^T(g)) when NV >= NS - 1.
+  static_assert(NK >= NS, "S_FULL reuse");
+  static_assert(NV >= NS - 1, "O_DONE reuse");
+  static_assert(OFF_Q % 1024 == 0, "the swizzled query tile starts on a 1024-byte boundary");
+  static_assert(D + NS * BN + (QS ? 0 : D / E::PER_WORD) <= static_cast<int>(kTmemCols), "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <int D, int BN, int NK, int NV, bool F8 = false, int NS = 2>
+template <int D, int BN, int NK, int NV, bool F8 = false, int NS = 2, bool QS = false>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const FwdParams p) {
-  using Cf = FwdCfg<D, BN, NK, NV, F8, NS>;
+  using Cf = FwdCfg<D, BN, NK, NV, F8, NS, QS>;
   using E = Elem<F8>;
   // launched as a programmatic dependent of the work-list grid: the prologue
   // (barriers, TMEM, descriptor prefetch) overlaps that grid, and nothing it
@@ -654,12 +671,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   // V_EMPTY; measured 1.5% faster there than freeing them through the MMA
   // warp's S_FULL / O_DONE commits, which the larger tiles use.  (It relies
   // on P.V running one tile behind QK^T: two S/P buffers.)
-  constexpr bool soft_release = (BN == 64);
-  static_assert(!soft_release || NS == 2, "soft release with two S/P buffers");
+  constexpr bool soft_release = (BN == 64) && (NS == 2);
   constexpr int LA = NS - 1;  // P.V of tile g is issued after QK^T of tile g + LA
 
   const uint32_t sK = sbase + Cf::OFF_K;
   const uint32_t sV = sbase + Cf::OFF_V;
+  const uint32_t sQ = sbase + Cf::OFF_Q;
   const uint32_t bars = sbase + Cf::OFF_BAR;
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + Cf::OFF_MISC);
@@ -729,7 +746,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // and box issues run side by side instead of one after the other.
     const bool is_k = (warp == kTmaWarp);
     const bool paged = p.block_table != nullptr;
-    const int NS = is_k ? NK : NV;
+    const int NR = is_k ? NK : NV;  // stages of this ring
     const uint32_t full0 = bar(is_k ? Cf::B_K_FULL : Cf::B_V_FULL);
     // a stage is free once its tile's QK^T (K) or P.V (V) is done
     const uint32_t empty0 = soft_release ? bar(is_k ? Cf::B_K_EMPTY : Cf::B_V_EMPTY)
@@ -773,7 +790,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           break;
         }
         if (is_k && loads++ == p.debug_skip_k_load) {
-          if (++stage == static_cast<uint32_t>(NS)) { stage = 0; phase ^= 1; }
+          if (++stage == static_cast<uint32_t>(NR)) { stage = 0; phase ^= 1; }
           continue;
         }
         // the expected bytes are registered before any box of the stage is issued
@@ -800,18 +817,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           ok_box = ok_box &&
                    in_bounds(row >= 0 && row < p.kv_rows && td.kvh >= 0 && td.kvh < p.Hkv &&
                                  (bk + 1) * E::BLK <= D && (dst & 1023u) == 0u &&
-                                 dst + static_cast<uint32_t>(box_rows * 128) <= ring + NS * Cf::KV_BYTES,
+                                 dst + static_cast<uint32_t>(box_rows * 128) <= ring + NR * Cf::KV_BYTES,
                              p.status, abort_flag);
           if (ok_box) tma_load_3d(dst, map, full0 + 8u * stage, bk * E::BLK, td.kvh, row);
         }
         issued_mask |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-        if (++stage == static_cast<uint32_t>(NS)) { stage = 0; phase ^= 1; }
+        if (++stage == static_cast<uint32_t>(NR)) { stage = 0; phase ^= 1; }
       }
     }
     if (!ok) {
       // let loads already in flight land before the CTA's shared memory goes away
-      for (int st = 0; st < NS; ++st)
+      for (int st = 0; st < NR; ++st)
         if (issued_mask & (1u << st)) drain_wait(full0 + 8u * st, (issued_phase >> st) & 1);
     }
     __syncwarp();
@@ -857,7 +874,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 #pragma unroll
             for (int kb = 0; kb < Cf::NKB; ++kb) {
               const uint64_t b = smem_desc_sw128(k_base + kb * (BN * 128), 16, 1024);
-              umma_ts_batch_warp<F8, 4>(d_s, tmem + Cf::TM_Q + kb * 32, b, idesc_qk, kb > 0 ? 1u : 0u, 8u, 2ull);
+              if constexpr (QS) {
+                // A from the query tile in shared memory: 32 bytes per K step
+                const uint64_t a = smem_desc_sw128(sQ + kb * (kRows * 128), 16, 1024);
+                umma_ss_batch4_warp<F8>(d_s, a, b, idesc_qk, kb > 0 ? 1u : 0u, 2ull, 2ull);
+              } else {
+                umma_ts_batch_warp<F8, 4>(d_s, tmem + Cf::TM_Q + kb * 32, b, idesc_qk, kb > 0 ? 1u : 0u, 8u,
+                                          2ull);
+              }
             }
             umma_commit_warp(bar(Cf::B_S_FULL + k_stage));
             if (++k_stage == NK) { k_stage = 0; k_phase ^= 1; }
@@ -933,12 +957,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         qw[4 * e + 0] = x.x; qw[4 * e + 1] = x.y; qw[4 * e + 2] = x.z; qw[4 * e + 3] = x.w;
       }
     };
-    // registers -> TMEM Q columns; the MMA warp may start QK^T after this
+    // registers -> Q (its TMEM columns, or with QS the shared-memory tile);
+    // the MMA warp may start QK^T after this
     auto q_commit = [&]() {
+      if constexpr (QS) {
+        // row r of each 128-byte column block, its 16-byte chunks placed by the
+        // 128-byte swizzle (chunk c of row r at position c ^ (r % 8)), then
+        // made visible to the tensor core's (async) proxy
+        uint8_t* qrow = sptr + Cf::OFF_Q + r * 128;
 #pragma unroll
-      for (int c = 0; c < kQW / 32; ++c)
-        tmem_st32(lane_base + Cf::TM_Q + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&qw[c * 32]));
-      tc_fence_before();
+        for (int kb = 0; kb < Cf::NKB; ++kb)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(qrow + kb * (kRows * 128) + ((c ^ (r & 7)) << 4)) =
+                make_uint4(qw[kb * 32 + 4 * c], qw[kb * 32 + 4 * c + 1], qw[kb * 32 + 4 * c + 2],
+                           qw[kb * 32 + 4 * c + 3]);
+        fence_proxy_async_smem();
+      } else {
+#pragma unroll
+        for (int c = 0; c < kQW / 32; ++c)
+          tmem_st32(lane_base + Cf::TM_Q + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&qw[c * 32]));
+        tc_fence_before();
+      }
       mbar_arrive(bar(Cf::B_Q_FULL));
     };
     Seg sg;
@@ -950,7 +990,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // With head_dim 256 the register file has room to stage the next row
     // during the epilogue; smaller head dims load it at the segment start.
     constexpr bool kStageQ = (D == 256);
-    bool q_loaded = true;  // the first segment's Q is already in TMEM
+    bool q_loaded = true;  // the first segment's Q is already committed
     while (ok && have) {
       const TileDesc td = p.ws.tiles[sg.tile];
       if (!q_loaded) {
@@ -1078,10 +1118,19 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
-      // PV(g_last) done implies every earlier MMA of this CTA is done
+      // PV(g_last) done implies every earlier MMA of this CTA is done.  A
+      // parity wait on O_DONE[x % NV] is only sound once PV(x - NV), the
+      // previous commit on that barrier, is done.  S(g_last) seen implies
+      // PV(g_last - NS) done; with NV < NS, PV(g_last - 1) is waited for first,
+      // which implies PV(g_last - NV) for any NV >= 1.
       {
         const uint32_t x = gj + n - 1;
-        if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_O_DONE + x % NV), (x / NV) & 1, abort_flag, p.status))) {
+        bool w = true;
+        if constexpr (NV < NS) {
+          if (x >= 1) w = wait_phase(bar(Cf::B_O_DONE + (x - 1) % NV), ((x - 1) / NV) & 1, abort_flag, p.status);
+        }
+        if (!__all_sync(0xffffffffu,
+                        w && wait_phase(bar(Cf::B_O_DONE + x % NV), (x / NV) & 1, abort_flag, p.status))) {
           ok = false;
           break;
         }

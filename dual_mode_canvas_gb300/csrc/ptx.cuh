@@ -200,6 +200,36 @@ __device__ __forceinline__ void umma_ts_batch_warp(uint32_t d_tmem, uint32_t a_t
 #undef DG_UMMA_X2
 #undef DG_UMMA_X4
 
+// Four MMAs of one batch with both operands in shared memory (SS form): the
+// k-th reads A through a_desc + k * a_step and B through b_desc + k * b_step
+// (descriptor units: 16 bytes of start address).  The first one overwrites D
+// when accumulate == 0, the others always accumulate.
+#define DG_UMMA_SS_X4(KIND)                                                                    \
+  "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"                            \
+  "elect.sync _|e, 0xffffffff;\n\t"                                                           \
+  "setp.ne.b32 p, %4, 0;\n\t"                                                                 \
+  "setp.eq.b32 t, %4, %4;\n\t"                                                                \
+  "add.s64 b1, %2, %6;\n\tadd.s64 b2, b1, %6;\n\tadd.s64 b3, b2, %6;\n\t"                     \
+  "add.s64 a1, %1, %5;\n\tadd.s64 a2, a1, %5;\n\tadd.s64 a3, a2, %5;\n\t"                     \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], %1, %2, %3, p;\n\t"                      \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], a1, b1, %3, t;\n\t"                      \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], a2, b2, %3, t;\n\t"                      \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], a3, b3, %3, t;\n\t}"
+
+template <bool F8>
+__device__ __forceinline__ void umma_ss_batch4_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                    uint32_t idesc, uint32_t accumulate, uint64_t a_step,
+                                                    uint64_t b_step) {
+  if constexpr (F8) {
+    asm volatile(DG_UMMA_SS_X4("f8f6f4") ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                 "l"(a_step), "l"(b_step) : "memory");
+  } else {
+    asm volatile(DG_UMMA_SS_X4("f16") ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                 "l"(a_step), "l"(b_step) : "memory");
+  }
+}
+#undef DG_UMMA_SS_X4
+
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
