@@ -203,6 +203,26 @@ dg_status_t encode_map(CUtensorMap* map, const void* base, int rows, int heads, 
   return r == CUDA_SUCCESS ? DG_OK : DG_ERR_INVALID_ARG;
 }
 
+// The paged V pool as a 4-D map {128-byte block of D, heads, rows, column
+// blocks of D} (the last stride, 128 bytes, is the smallest: it walks the
+// column blocks of one row), box {one block, one head, box_rows, every column
+// block}: one box is a whole page of one head, landing as [column block][row].
+dg_status_t encode_page_map(CUtensorMap* map, const void* base, int rows, int heads, int D, int box_rows,
+                            bool e4m3) {
+  const cuuint64_t es = e4m3 ? 1 : 2;
+  const cuuint64_t nkb = static_cast<cuuint64_t>(D) * es / 128;
+  const cuuint64_t dims[4] = {128 / es, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows), nkb};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * es, static_cast<cuuint64_t>(heads) * D * es, 128};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), 1u, static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(nkb)};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = g_encode(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DG_OK : DG_ERR_INVALID_ARG;
+}
+
 template <int D, bool F8 = false>
 dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
                    const FwdParams& p, int num_ctas, int max_tiles, cudaStream_t stream,
@@ -323,8 +343,15 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   const void* kmap = pg ? pg->k_cache : k;
   const void* vmap = pg ? pg->v_cache : v;
   const int map_rows = pg ? (pg->num_pages << pg->page_shift) : total_kv;
+  // V pages of exactly one MMA K step, and head_dim over several 128-byte
+  // blocks: one box per page (DG_ATTN_V_PAGE_BOX=0 keeps a box per block)
+  const int kstep = f8 ? 32 : 16;
+  const int nkb = head_dim * (f8 ? 1 : 2) / 128;
+  const char* vpb_env = std::getenv("DG_ATTN_V_PAGE_BOX");
+  const bool v_page_box = pg && box == kstep && box < BN && nkb > 1 && !(vpb_env && std::strcmp(vpb_env, "0") == 0);
   if (encode_map(&mk, kmap, map_rows, num_kv_heads, head_dim, 1, box, f8) != DG_OK ||
-      encode_map(&mv, vmap, map_rows, num_kv_heads, head_dim, 1, box, f8) != DG_OK)
+      (v_page_box ? encode_page_map(&mv, vmap, map_rows, num_kv_heads, head_dim, box, f8)
+                  : encode_map(&mv, vmap, map_rows, num_kv_heads, head_dim, 1, box, f8)) != DG_OK)
     return DG_ERR_INVALID_ARG;
 
   uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -347,6 +374,10 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.block_table = pg ? pg->block_table : nullptr;
   p.page_shift = pg ? pg->page_shift : 0;
   p.page_box = box;
+  p.v_page_box = v_page_box ? 1 : 0;
+  // a K tile of 8 or more boxes: two warps issue them (DG_ATTN_K_SPLIT=0: one)
+  const char* ks_env = std::getenv("DG_ATTN_K_SPLIT");
+  p.k_split = ((BN / box) * nkb >= 8 && !(ks_env && std::strcmp(ks_env, "0") == 0)) ? 1 : 0;
   p.debug_skip_k_load = -1;
   if (const char* e = std::getenv("DG_ATTN_DEBUG_SKIP_K_LOAD")) p.debug_skip_k_load = std::atoi(e);
   p.Hkv = num_kv_heads;

@@ -43,10 +43,11 @@
 namespace dg {
 
 constexpr int kRows = 128;          // query rows per tile (UMMA M, TMEM lanes)
-constexpr int kThreads = 224;       // 4 softmax warps + K loader + MMA issuer + V loader
+constexpr int kThreads = 256;       // 4 softmax warps + K loader + MMA issuer + V loader + K loader 2
 constexpr int kTmaWarp = 4;         // loads the K ring
 constexpr int kMmaWarp = 5;         // issues tcgen05 MMAs, owns TMEM
 constexpr int kVLoadWarp = 6;       // loads the V ring
+constexpr int kTmaWarp2 = 7;        // with k_split, issues half of every K tile's boxes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitTimeoutNs = 250ull * 1000ull * 1000ull;
 // Work-split weight of starting a segment (Q load, pipeline fill, epilogue),
@@ -113,6 +114,19 @@ struct FwdParams {
   // pages of 2^page_shift rows, TMA boxes of page_box rows
   const int32_t* block_table;
   int page_shift, page_box;
+  // 1: the V tensor map is 4-D ({128-byte block, head, row, column block})
+  // and one box brings a whole page (page_box rows, every column block of
+  // head_dim): a page of one MMA K step (16 bf16 / 32 e4m3 rows) lands as
+  // [column block][row][128 bytes], which P.V reads with the column-block
+  // stride of one page.  Cuts a 16-row-page V tile from NKB boxes per page to
+  // one.  (K cannot: QK^T's B operand needs every key row of a column block at
+  // one stride.)
+  int v_page_box;
+  // 1: two warps issue a K tile's TMA boxes, half each (each registers its
+  // half of the bytes on K_FULL, which then counts two arrivals).  A K tile of
+  // small pages is 16 or more boxes, and one warp issuing them one after the
+  // other is what paces the loads (~75 clocks a box).
+  int k_split;
   // >= 0: the K loader skips the TMA load of this (per-CTA) KV tile, so the
   // MMA warp's bounded wait for it expires (tests of the timeout path)
   int debug_skip_k_load;
@@ -689,7 +703,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // since the next tile on the same barrier, x + NK (x + NV), cannot be
     // issued before P(x) exists.
     for (int s = 0; s < NK; ++s) {
-      mbar_init(bar(Cf::B_K_FULL + s), 1);
+      mbar_init(bar(Cf::B_K_FULL + s), p.k_split ? 2 : 1);
       mbar_init(bar(Cf::B_S_FULL + s), 1);
       mbar_init(bar(Cf::B_K_EMPTY + s), 1);
     }
@@ -737,14 +751,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   SegIter it{p.ws.unit_begin, num_tiles, u_beg, u_end, cta, true};
   const int G = p.G, TT = p.TT;
 
-  if (warp == kTmaWarp || warp == kVLoadWarp) {
+  if (warp == kTmaWarp || warp == kVLoadWarp || (warp == kTmaWarp2 && p.k_split)) {
     // ----------------------------------------------------------- producers
-    // Warp 4 loads the K ring, warp 6 the V ring, each from this GPU's
-    // memory into this CTA's shared memory.  The whole warp runs the loop
-    // with warp-uniform control flow; the TMA boxes of one KV tile are spread
-    // over the lanes, one box per lane, so that a paged tile's page lookups
-    // and box issues run side by side instead of one after the other.
-    const bool is_k = (warp == kTmaWarp);
+    // Warp 4 (with k_split, warps 4 and 7) loads the K ring, warp 6 the V
+    // ring, each from this GPU's memory into this CTA's shared memory.  The
+    // whole warp runs the loop with warp-uniform control flow; the TMA boxes
+    // of one KV tile are spread over the lanes, one box per lane, so that a
+    // paged tile's page lookups and box issues run side by side instead of
+    // one after the other.
+    const bool is_k = (warp != kVLoadWarp);
+    const int nkw = is_k && p.k_split ? 2 : 1;       // warps sharing this ring's boxes
+    const int kw = (warp == kTmaWarp2) ? 1 : 0;       // this warp's share
     const bool paged = p.block_table != nullptr;
     const int NR = is_k ? NK : NV;  // stages of this ring
     const uint32_t full0 = bar(is_k ? Cf::B_K_FULL : Cf::B_V_FULL);
@@ -757,9 +774,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // (at most 32: a box holds at least 8 rows, BN * NKB <= 256)
     const int box_rows = paged ? p.page_box : BN;
     const int nbr = BN / box_rows;
-    const bool has_box = lane < nbr * Cf::NKB;
-    const int br = lane % nbr, bk = lane / nbr;
-    const uint32_t box_off = static_cast<uint32_t>(bk * (BN * 128) + br * box_rows * 128);
+    const bool page_box = !is_k && p.v_page_box;  // one box per page, every column block
+    const int box_i = lane * nkw + kw;              // boxes interleaved over the warps
+    const bool has_box = box_i < (page_box ? nbr : nbr * Cf::NKB);
+    const int br = page_box ? box_i : box_i % nbr, bk = page_box ? 0 : box_i / nbr;
+    const uint32_t box_off = page_box ? static_cast<uint32_t>(br * (Cf::NKB * box_rows * 128))
+                                      : static_cast<uint32_t>(bk * (BN * 128) + br * box_rows * 128);
+    const uint32_t box_bytes = static_cast<uint32_t>((page_box ? Cf::NKB : 1) * box_rows * 128);
     const int pmask = (1 << p.page_shift) - 1;
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;  // per stage: a load was issued / its phase
@@ -768,7 +789,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     Seg sg;
     while (ok && it.next(sg)) {
       const TileDesc td = p.ws.tiles[sg.tile];
-      if (is_k) {
+      if (is_k && kw == 0) {
         // the next segment's Q rows go to L2 while this segment streams, so
         // the softmax warps load them at L2 latency at the segment switch
         SegIter look = it;
@@ -784,7 +805,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       // positions past the sequence's last key read its last page (checked
       // by the work-list launch); the softmax masks them
       const int last_page = (td.L - 1) >> p.page_shift;
+      // This lane's page-table entry for KV tile j; the one for tile j + 1 is
+      // read one iteration ahead, so its latency overlaps this tile's wait
+      // and box issue (with 16-row pages the issue of a K tile's 16 boxes is
+      // what paces the loader).
+      auto page_entry = [&](int j, bool& ok_ent) -> int {
+        const int pos = kv_tile(td, j) * BN + br * box_rows;
+        const int64_t ent = static_cast<int64_t>(td.kv_row0) + min(pos >> p.page_shift, last_page);
+        ok_ent = in_bounds(ent >= 0 && ent < p.bt_entries, p.status, abort_flag);
+        return ok_ent ? __ldg(p.block_table + ent) : 0;
+      };
+      bool ok_next = true;
+      int page_next = (paged && has_box && sg.j0 < sg.j1) ? page_entry(sg.j0, ok_next) : 0;
       for (int j = sg.j0; j < sg.j1; ++j) {
+        const int page_cur = page_next;
+        const bool ok_cur = ok_next;
+        if (paged && has_box && j + 1 < sg.j1) page_next = page_entry(j + 1, ok_next);
         if (!__all_sync(0xffffffffu, wait_phase(empty0 + 8u * stage, phase ^ 1, abort_flag, p.status))) {
           ok = false;
           break;
@@ -794,7 +830,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           continue;
         }
         // the expected bytes are registered before any box of the stage is issued
-        if (lane == 0) mbar_arrive_expect_tx(full0 + 8u * stage, static_cast<uint32_t>(Cf::KV_BYTES));
+        if (lane == 0) mbar_arrive_expect_tx(full0 + 8u * stage, static_cast<uint32_t>(Cf::KV_BYTES / nkw));
         __syncwarp();
         if (has_box) {
           const int pos = kv_tile(td, j) * BN + br * box_rows;
@@ -803,10 +839,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           if (!paged) {
             row = td.kv_row0 + pos;
           } else {
-            const int64_t ent = static_cast<int64_t>(td.kv_row0) + min(pos >> p.page_shift, last_page);
-            ok_box = in_bounds(ent >= 0 && ent < p.bt_entries, p.status, abort_flag);
-            const int page = ok_box ? __ldg(p.block_table + ent) : 0;
-            row = (page << p.page_shift) + (pos & pmask);
+            ok_box = ok_cur;
+            row = (page_cur << p.page_shift) + (pos & pmask);
           }
           if constexpr (kBoundsChecks) {
             if (is_k && loads - 1 == p.debug_bad_kv_row) row += p.kv_rows;
@@ -817,9 +851,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           ok_box = ok_box &&
                    in_bounds(row >= 0 && row < p.kv_rows && td.kvh >= 0 && td.kvh < p.Hkv &&
                                  (bk + 1) * E::BLK <= D && (dst & 1023u) == 0u &&
-                                 dst + static_cast<uint32_t>(box_rows * 128) <= ring + NR * Cf::KV_BYTES,
+                                 dst + box_bytes <= ring + NR * Cf::KV_BYTES,
                              p.status, abort_flag);
-          if (ok_box) tma_load_3d(dst, map, full0 + 8u * stage, bk * E::BLK, td.kvh, row);
+          if (ok_box) {
+            if (page_box) tma_load_4d(dst, map, full0 + 8u * stage, 0, td.kvh, row, 0);
+            else tma_load_3d(dst, map, full0 + 8u * stage, bk * E::BLK, td.kvh, row);
+          }
         }
         issued_mask |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -855,6 +892,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       int seg_i = 0;
       bool ok = true;
       bool k_ready = false;  // the next QK's K stage was seen full by the last probe
+      // V tile layout: [column block][BN rows][128 B] (column blocks BN * 128
+      // bytes apart, a K step KSTEP rows further on), or with whole-page
+      // boxes [page][column block][KSTEP rows][128 B] (a page per K step)
+      const uint32_t pv_lbo = p.v_page_box ? E::KSTEP * 128 : BN * 128;
+      const uint32_t pv_step_bytes = p.v_page_box ? Cf::NKB * E::KSTEP * 128 : E::KSTEP * 128;
       Seg sg;
       while (ok && it.next(sg)) {
         if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_Q_FULL), seg_i & 1, abort_flag, p.status))) { ok = false; break; }
@@ -909,10 +951,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             static_assert(kPvSteps % kPvBatch == 0, "P.V steps in batches of 2 or 4");
 #pragma unroll
             for (int kb = 0; kb < kPvSteps / kPvBatch; ++kb) {
-              const uint64_t b = smem_desc_sw128(v_base + kb * kPvBatch * (E::KSTEP * 128), BN * 128, 1024);
+              const uint64_t b = smem_desc_sw128(v_base + kb * kPvBatch * pv_step_bytes, pv_lbo, 1024);
               umma_ts_batch_warp<F8, kPvBatch>(tmem + Cf::TM_O, p_tm + kb * kPvBatch * 8, b, idesc_pv,
                                                (first && kb == 0) ? 0u : 1u, 8u,
-                                               static_cast<uint64_t>(E::KSTEP * 128 / 16));
+                                               static_cast<uint64_t>(pv_step_bytes / 16));
             }
             umma_commit_warp(bar(Cf::B_O_DONE + v_stage));
             if (++v_stage == NV) { v_stage = 0; v_phase ^= 1; }

@@ -97,13 +97,16 @@ def _bits(t):
     return t.cpu().view(torch.int16).numpy()
 
 
+@pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("P", [8, 16, 64])
-def test_paged_equals_contiguous_bit_for_bit(P):
+def test_paged_equals_contiguous_bit_for_bit(P, D):
     """The same keys laid out contiguously (gathered through the page table by
     the oracle's gather) give bit-identical outputs through dg_attn_forward:
     both calls split the work the same way and differ only in where each TMA
-    box of a KV tile comes from."""
-    wl = wls.Workload("paged", ((300, 256, 1), (0, 333, 0), (1000, 200, 1)), 8, 4, 128, -1, 77)
+    box of a KV tile comes from (16-row pages: one V box per page, read by P.V
+    with the page's column-block stride)."""
+    Hq, Hkv = (8, 4) if D == 128 else (16, 2)
+    wl = wls.Workload("paged", ((300, 256, 1), (0, 333, 0), (1000, 200, 1)), Hq, Hkv, D, -1, 77)
     b = wls.make_paged_batch(wl, P, device="cuda")
     d = to_dev(b)
     out_p, lse_p = run_paged(d, -1, wl.scale)
@@ -120,6 +123,23 @@ def test_paged_equals_contiguous_bit_for_bit(P):
     assert binding.status() == binding.DG_OK
     assert torch.equal(out_p, out_c)
     assert torch.equal(lse_p, lse_c)
+
+
+@pytest.mark.parametrize("knob", ["DG_ATTN_V_PAGE_BOX", "DG_ATTN_K_SPLIT"])
+@pytest.mark.parametrize("D", [128, 256])
+def test_box_layouts_give_the_same_bits(D, knob, monkeypatch):
+    """16-row pages: the default loads (V as one box per page, a K tile's boxes
+    issued by two warps) and the plain ones (a V box per page and 128-byte
+    column block; one K warp) give the same bits."""
+    Hq, Hkv = (8, 4) if D == 128 else (16, 2)
+    wl = wls.Workload("vbox", ((700, 256, 1), (0, 190, 0)), Hq, Hkv, D, -1, 78)
+    b = wls.make_paged_batch(wl, 16, device="cuda")
+    d = to_dev(b)
+    out_a, lse_a = run_paged(d, -1, wl.scale, append=False)
+    monkeypatch.setenv(knob, "0")
+    out_b, lse_b = run_paged(d, -1, wl.scale, append=False)
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(lse_a, lse_b)
 
 
 def test_rows_already_in_the_cache():
