@@ -232,7 +232,7 @@ dg_status_t launch(const CUtensorMap& mk, const CUtensorMap& mv,
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DG_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(p.k_split ? kThreads : kThreads - 32);  // warp 7 only with k_split
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -378,6 +378,14 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   // a K tile of 8 or more boxes: two warps issue them (DG_ATTN_K_SPLIT=0: one)
   const char* ks_env = std::getenv("DG_ATTN_K_SPLIT");
   p.k_split = ((BN / box) * nkb >= 8 && !(ks_env && std::strcmp(ks_env, "0") == 0)) ? 1 : 0;
+  // segment weight in KV-tile units: a segment (Q load, pipeline fill,
+  // epilogue) costs about the same time at every head_dim, a 64-key tile of
+  // head_dim 256 less than a 128-key one.  Measured optima: 18 for head_dim 256
+  // (denoise loop 0.1698 vs 0.1732 ms at 8, e4m3 0.1356 vs 0.1375 ms), 8 for
+  // head_dim 128 (mixed batch 43.3 us; 4 / 14: 46.3 / 45.1 us).
+  // DG_ATTN_SEG_WEIGHT overrides it.
+  p.seg_weight = head_dim == 256 ? 18 : 8;
+  if (const char* e = std::getenv("DG_ATTN_SEG_WEIGHT")) p.seg_weight = std::max(0, std::atoi(e));
   p.debug_skip_k_load = -1;
   if (const char* e = std::getenv("DG_ATTN_DEBUG_SKIP_K_LOAD")) p.debug_skip_k_load = std::atoi(e);
   p.Hkv = num_kv_heads;
@@ -408,7 +416,7 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.num_slots = 2 * num_ctas;
   build_worklist_kernel<<<1 + append_ctas, 1024, 0, stream>>>(
       cu_q, ctx_len, mode, num_seqs, total_q, pg ? INT32_MAX : total_kv, num_kv_heads, TT, BN,
-      window, lay.max_tiles, num_ctas, rotate_kv_order() ? 1 : 0, p.ws, pa, p.status);
+      window, lay.max_tiles, num_ctas, rotate_kv_order() ? 1 : 0, p.seg_weight, p.ws, pa, p.status);
   if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
   cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
   if (f8) {

@@ -43,7 +43,7 @@
 namespace dg {
 
 constexpr int kRows = 128;          // query rows per tile (UMMA M, TMEM lanes)
-constexpr int kThreads = 256;       // 4 softmax warps + K loader + MMA issuer + V loader + K loader 2
+constexpr int kThreads = 256;       // 4 softmax warps + K loader + MMA issuer + V loader (+ K loader 2)
 constexpr int kTmaWarp = 4;         // loads the K ring
 constexpr int kMmaWarp = 5;         // issues tcgen05 MMAs, owns TMEM
 constexpr int kVLoadWarp = 6;       // loads the V ring
@@ -51,9 +51,10 @@ constexpr int kTmaWarp2 = 7;        // with k_split, issues half of every K tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitTimeoutNs = 250ull * 1000ull * 1000ull;
 // Work-split weight of starting a segment (Q load, pipeline fill, epilogue),
-// in KV-tile units: every tile occupies kSegWeight + (its KV tiles) units of
-// the split, the first kSegWeight of them carrying no KV tile.
-constexpr int kSegWeight = 8;
+// in KV-tile units: every tile occupies seg_weight + (its KV tiles) units of
+// the split, the first seg_weight of them carrying no KV tile.  The host
+// picks it per kernel shape (a segment costs about the same time whatever the
+// shape, a KV tile does not).
 
 // error codes shared with the host (same values as dg_status_t)
 constexpr int kErrInvalid = 1;
@@ -127,6 +128,7 @@ struct FwdParams {
   // small pages is 16 or more boxes, and one warp issuing them one after the
   // other is what paces the loads (~75 clocks a box).
   int k_split;
+  int seg_weight;  // the work list's segment weight (KV-tile units)
   // >= 0: the K loader skips the TMA load of this (per-CTA) KV tile, so the
   // MMA warp's bounded wait for it expires (tests of the timeout path)
   int debug_skip_k_load;
@@ -317,7 +319,7 @@ constexpr int kWlSmemSeqs = 1024;
 __global__ void __launch_bounds__(1024, 1)
 build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ ctx_len,
                       const uint8_t* __restrict__ mode, int B, int total_q, int total_kv, int Hkv,
-                      int TT, int BN, int window, int max_tiles, int num_ctas, int rotate,
+                      int TT, int BN, int window, int max_tiles, int num_ctas, int rotate, int seg_weight,
                       Workspace ws, PagedArgs pg, int* status) {
   // the attention kernel is launched as a programmatic dependent: its CTAs
   // become resident while this grid runs and wait for it to finish
@@ -453,14 +455,14 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
   };
   // pass 1: the units of this thread's tiles, scanned over the block
   int64_t mine = 0;
-  for (int t = t_begin; t < t_end; ++t) mine += kSegWeight + make_tile(t).kt_count;
+  for (int t = t_begin; t < t_end; ++t) mine += seg_weight + make_tile(t).kt_count;
   int64_t U;
   int64_t ub = block_scan_1024(mine, &U);
   const int P = active_ctas(num_ctas, U);
   // pass 2: the finished descriptors, written once
   for (int t = t_begin; t < t_end; ++t) {
     TileDesc td = make_tile(t);
-    const int64_t r0 = ub + kSegWeight, n = td.kt_count;
+    const int64_t r0 = ub + seg_weight, n = td.kt_count;
     // CTAs holding KV tiles of this tile, and the partial slot of the first
     if (U > 0) {
       const int c_lo = cta_of_unit(r0, U, P), c_hi = cta_of_unit(r0 + n - 1, U, P);
@@ -481,7 +483,7 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
     }
     ws.tiles[t] = td;
     ws.unit_begin[t] = ub;
-    ub += kSegWeight + n;
+    ub += seg_weight + n;
   }
   if (tid == 0) {
     ws.unit_begin[num_tiles] = U;
@@ -510,18 +512,19 @@ struct Seg {
 
 // Walks the segments of one CTA's unit range; every role walks the same
 // list.  A query tile spans units [ub[t], ub[t+1]); its KV tiles are the units
-// from ub[t] + kSegWeight on, so a range that only touches a tile's first
-// kSegWeight units yields no segment of it.
+// from ub[t] + seg_w on, so a range that only touches a tile's first seg_w
+// units yields no segment of it.
 struct SegIter {
   const int64_t* ub;
   int num_tiles;
   int64_t u, u_end;
   int cta;
   bool first;
+  int seg_w;
   __device__ bool next(Seg& sg) {
     while (u < u_end) {
       const int t = tile_of_unit(ub, num_tiles, u);
-      const int64_t r0 = ub[t] + kSegWeight, t1 = ub[t + 1];
+      const int64_t r0 = ub[t] + seg_w, t1 = ub[t + 1];
       const int64_t b = u > r0 ? u : r0;
       const int64_t e = u_end < t1 ? u_end : t1;
       u = e;
@@ -748,7 +751,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   const int64_t u_beg = active ? cta_unit_begin(cta, U, P) : 0;
   const int64_t u_end = active ? cta_unit_begin(cta + 1, U, P) : 0;
 
-  SegIter it{p.ws.unit_begin, num_tiles, u_beg, u_end, cta, true};
+  SegIter it{p.ws.unit_begin, num_tiles, u_beg, u_end, cta, true, p.seg_weight};
   const int G = p.G, TT = p.TT;
 
   if (warp == kTmaWarp || warp == kVLoadWarp || (warp == kTmaWarp2 && p.k_split)) {
