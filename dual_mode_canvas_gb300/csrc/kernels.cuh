@@ -905,6 +905,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         if (!__all_sync(0xffffffffu, wait_phase(bar(Cf::B_Q_FULL), seg_i & 1, abort_flag, p.status))) { ok = false; break; }
         tc_fence_after();
         const int n = sg.j1 - sg.j0;
+        // e4m3: the loop body twice per iteration (measured: denoise loop
+        // 0.1347 vs 0.1358 ms, max mix 0.697 vs 0.709 ms; bf16 was slower so)
+        constexpr int kMmaUnroll = F8 ? 2 : 1;
+#pragma unroll kMmaUnroll
         for (int jj = 0; jj < n + LA && ok; ++jj) {
           if (jj < n) {
             const uint32_t g = gj + jj;
