@@ -138,6 +138,20 @@ def test_grid_sizes(ctas):
         del os.environ["DG_ATTN_NUM_CTAS"]
 
 
+@pytest.mark.parametrize("weight", ["0", "3", "40"])
+def test_segment_weights(weight, monkeypatch):
+    """The work split's segment weight moves every CTA boundary (0: KV
+    tiles only; 40: a tile start outweighs most of its KV tiles): each split
+    gives the oracle's result, at head_dim 128 and 256."""
+    monkeypatch.setenv("DG_ATTN_SEG_WEIGHT", weight)
+    for seed, seqs, Hq, Hkv, D in ((44, ((300, 256, 1), (0, 333, 0), (1000, 200, 1)), 8, 4, 128),
+                                   (45, ((700, 256, 1), (5, 100, 0)), 16, 2, 256)):
+        wl, batch = wls.random_batch(seed, seqs, Hq, Hkv, D, -1)
+        dev = to_dev(batch)
+        for W in (-1, 129):
+            full_check(wl, batch, window=W, dev=dev, rel=EDGE_REL)
+
+
 @pytest.mark.parametrize("D", [128, 256])
 def test_large_logits(D):
     """A large softmax scale spreads the scores over hundreds of units: the row
