@@ -672,9 +672,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   // launched as a programmatic dependent of the work-list grid: the prologue
   // (barriers, TMEM, descriptor prefetch) overlaps that grid, and nothing it
   // wrote is read before it has finished.  The split-KV merge is this grid's
-  // own dependent: it may launch at once and become resident as CTAs of this
-  // grid exit; it waits for this grid before reading the partials.
-  griddep_launch_dependents();
+  // own dependent, released once every CTA has passed that wait (so the work
+  // list is complete when the merge starts); it becomes resident as CTAs of
+  // this grid exit and waits for this grid before reading the partials.
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -740,6 +740,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   in_bounds(tmem == 0u, p.status, abort_flag);
 
   griddep_wait();
+  griddep_launch_dependents();
   const WorkHeader* hdr = p.ws.hdr;
   const int num_tiles = hdr->num_tiles;
   const int64_t U = hdr->total_units;
@@ -1263,14 +1264,15 @@ combine_kernel(const FwdParams p) {
   const int r = blockIdx.y * kCombineWarps + warp;
   if (r >= G * p.TT) return;
   const int t = r / G, gi = r - t * G;
-  // the tile table and the partials are written by the preceding grids
-  griddep_wait();
-  // both loads issued together (the descriptor of a tile past num_tiles is
-  // stale but lies inside the workspace and is not used)
+  // The tile table was complete before the attention grid released this
+  // grid, so it is read before the wait; only the partials wait for the
+  // attention grid.  Both loads issued together (the descriptor of a tile
+  // past num_tiles is stale but lies inside the workspace and is not used).
   const int num_tiles = p.ws.hdr->num_tiles;
   const TileDesc td = p.ws.tiles[tile];
   if (tile >= num_tiles || td.comb_n <= 1) return;  // no tile, or written directly by one CTA
   if (t >= td.n_tok) return;
+  griddep_wait();
   const int nc = td.comb_n;
   // partial slot of contributor i: the first CTA's is recorded, the others
   // hold the tile in their first segment
