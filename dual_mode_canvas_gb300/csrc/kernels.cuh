@@ -6,15 +6,17 @@
 //                          range is the union of the rows' windows (causal:
 //                          keys <= i, bidirectional: the whole sequence, both
 //                          narrowed to [i-W, i+W] on sliding-window layers).
-//   fwd_kernel<D,BN,NK,NV> persistent, one CTA per SM.  The (tile, KV-tile)
-//                          work units are split evenly over the CTAs; every
-//                          CTA TMA-loads the K/V tiles it consumes from this
-//                          GPU's memory into its own shared memory.  A tile cut
-//                          between CTAs leaves fp32 partials + LSE.
+//   fwd_kernel<D,BN,NK,NV,F8,NS,QS> persistent, one CTA per SM.  The (tile,
+//                          KV-tile) work units are split over the CTAs by
+//                          weight; every CTA TMA-loads the K/V tiles it
+//                          consumes from this GPU's memory into its own shared
+//                          memory.  A tile cut between CTAs leaves fp32
+//                          partials + LSE.
 //                          Warp roles: warps 4 and 6 issue TMA loads (K ring,
-//                          V ring), warp 5 issues tcgen05 MMAs, warps 0-3
-//                          (one TMEM lane = one query row each) stage Q in
-//                          TMEM and run the online softmax and the epilogue.
+//                          V ring; warp 7 shares the K boxes of tiles of small
+//                          pages), warp 5 issues tcgen05 MMAs, warps 0-3 (one
+//                          TMEM lane = one query row each) stage Q and run the
+//                          online softmax and the epilogue.
 //   combine_kernel<D>      merges the partials of cut tiles by their LSE.
 //
 // Paged KV cache (block-table indirection): K and V live in pools of pages of
@@ -23,7 +25,8 @@
 // launch then also appends the query tokens' K/V rows into their pages (CTAs
 // 1.. of the launch) and checks every page-table entry the attention will
 // read; the loaders look up each tile's pages and load them in boxes of
-// min(P, BN) rows, one box per lane of the loader warp.
+// min(P, BN) rows, one box per lane of the loader warp (V pages of one MMA K
+// step in one box per page).
 //
 // Rules (DiffusionGemma, agentlenshq page, "dual-mode operation", "dynamic
 // per-sequence causal attention", "symmetric sliding-window attention"): a

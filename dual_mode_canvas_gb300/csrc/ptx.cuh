@@ -152,17 +152,6 @@ __device__ __forceinline__ void umma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tm
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// The same with e4m3 A (from TMEM) and B (shared memory): kind::f8f6f4.
-__device__ __forceinline__ void umma_e4m3_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                  uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // N (2 or 4) MMAs of one batch in one asm block: one elect.sync for all of
 // them; the k-th (k = 0 .. N-1) reads A at a_tmem + k * a_step and B through
 // b_desc + k * b_step (descriptor units: 16 bytes of start address).  The
@@ -441,11 +430,5 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
 
 }  // namespace dg
