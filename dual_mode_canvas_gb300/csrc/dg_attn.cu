@@ -63,16 +63,19 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 //   query tile in shared memory with three 128-key buffers (0.827 vs 0.820 ms;
 //   at head_dim 256 the 64 KB query tile leaves five ring stages: denoise loop
 //   0.198 vs 0.172 ms).
-// - e4m3 tiles are half the bytes, so the same rings hold more stages, and
-//   three buffers pay: head_dim 256 has TMEM room for them (256 + 3 x 64 + 64
-//   columns; denoise loop 0.137 vs 0.145 ms), head_dim 128 moves its query tile
-//   to shared memory for them (max mix 0.691 vs 0.698 ms).
+// - e4m3 tiles are half the bytes, so the same rings hold more stages.
+//   head_dim 128 moves its query tile to shared memory for three buffers (max
+//   mix 0.691 vs 0.698 ms).  head_dim 256 moves it there for 128-key tiles with
+//   two buffers (256 + 2 x 128 columns; 3 K + 3 V stages of 32 KB and the 32 KB
+//   query tile): denoise loop 0.116 vs 0.134 ms with 64-key tiles and three
+//   buffers (which had beaten two 64-key buffers, 0.137 vs 0.145 ms); rings of
+//   4 + 2 or 2 + 4 stages time the same.
 template <int D, bool F8 = false> struct Shape;
 template <> struct Shape<64> { static constexpr int BN = 128, NK = 6, NV = 6, NS = 3; static constexpr bool QS = false; };
 template <> struct Shape<128> { static constexpr int BN = 128, NK = 4, NV = 3, NS = 2; static constexpr bool QS = false; };
 template <> struct Shape<256> { static constexpr int BN = 64, NK = 4, NV = 3, NS = 2; static constexpr bool QS = false; };
 template <> struct Shape<128, true> { static constexpr int BN = 128, NK = 6, NV = 6, NS = 3; static constexpr bool QS = true; };
-template <> struct Shape<256, true> { static constexpr int BN = 64, NK = 6, NV = 6, NS = 3; static constexpr bool QS = false; };
+template <> struct Shape<256, true> { static constexpr int BN = 128, NK = 3, NV = 3, NS = 2; static constexpr bool QS = true; };
 
 int kv_tile_rows(int D, bool f8 = false) {
   if (f8) return D == 128 ? Shape<128, true>::BN : Shape<256, true>::BN;
@@ -380,11 +383,13 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.k_split = ((BN / box) * nkb >= 8 && !(ks_env && std::strcmp(ks_env, "0") == 0)) ? 1 : 0;
   // segment weight in KV-tile units: a segment (Q load, pipeline fill,
   // epilogue) costs about the same time at every head_dim, a 64-key tile of
-  // head_dim 256 less than a 128-key one.  Measured optima: 18 for head_dim 256
-  // (denoise loop 0.1698 vs 0.1732 ms at 8, e4m3 0.1356 vs 0.1375 ms), 8 for
-  // head_dim 128 (mixed batch 43.3 us; 4 / 14: 46.3 / 45.1 us).
+  // head_dim 256 less than a 128-key one.  Measured optima: 18 for 64-key
+  // tiles (bf16 denoise loop 0.1698 vs 0.1732 ms at 8), 8 for 128-key tiles
+  // of head_dim 128 (mixed batch 43.3 us; 4 / 14: 46.3 / 45.1 us), 12 for the
+  // e4m3 128-key tiles of head_dim 256 (denoise loop 0.1155 ms; 5 / 8 / 18:
+  // 0.1183 / 0.1165 / 0.1160 ms).
   // DG_ATTN_SEG_WEIGHT overrides it.
-  p.seg_weight = head_dim == 256 ? 18 : 8;
+  p.seg_weight = BN == 64 ? 18 : (head_dim == 256 ? 12 : 8);
   if (const char* e = std::getenv("DG_ATTN_SEG_WEIGHT")) p.seg_weight = std::max(0, std::atoi(e));
   p.debug_skip_k_load = -1;
   if (const char* e = std::getenv("DG_ATTN_DEBUG_SKIP_K_LOAD")) p.debug_skip_k_load = std::atoi(e);

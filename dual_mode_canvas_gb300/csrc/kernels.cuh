@@ -1040,9 +1040,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       q_issue(p.ws.tiles[sg.tile]);
       q_commit();
     }
-    // With head_dim 256 the register file has room to stage the next row
-    // during the epilogue; smaller head dims load it at the segment start.
-    constexpr bool kStageQ = (D == 256);
+    // With head_dim 256 and Q in TMEM the register file has room to stage
+    // the next row during the epilogue; smaller head dims, and the shared-
+    // memory query tile of 128-key e4m3 tiles (whose staged row spilled), load
+    // it at the segment start.
+    constexpr bool kStageQ = (D == 256) && !QS;
     bool q_loaded = true;  // the first segment's Q is already committed
     while (ok && have) {
       const TileDesc td = p.ws.tiles[sg.tile];
