@@ -130,6 +130,31 @@ def test_grid_sizes(ctas):
         del os.environ["DG_ATTN_NUM_CTAS"]
 
 
+@pytest.mark.parametrize("weight", ["0", "40"])
+def test_segment_weights(weight, monkeypatch):
+    """The work split's segment weight moves every CTA boundary, so CTAs
+    switch tiles mid-range: each segment's query tile is loaded into shared
+    memory (head_dim 256) at its start, and each split gives the oracle's
+    result."""
+    monkeypatch.setenv("DG_ATTN_SEG_WEIGHT", weight)
+    b = wls.make_fp8_batch(wls.Workload("fp8", ((700, 256, 1), (5, 100, 0)), 16, 2, 256, -1, 77))
+    for W in (-1, 129):
+        out, lse = run_fp8(b, W)
+        check(out, lse, b, W, f"weight {weight} W={W}")
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_large_logits(D):
+    """A large softmax scale spreads the scores over hundreds of units: the
+    running maximum keeps growing across KV tiles, so the lazy O rescale
+    (every 2^3 of growth in e4m3) and the recomputed exponentials of rows
+    whose maximum moved run many times."""
+    b = wls.make_fp8_batch(wls.Workload("fp8", ((3000, 256, 1), (0, 400, 0)), 8, 2, D, -1, 76 + D))
+    b["scale"] = 1.5
+    out, lse = run_fp8(b, -1)
+    check(out, lse, b, -1, f"large logits D={D}")
+
+
 def test_denoise_loop_sampled():
     """One 256-query canvas over 32768 cached tokens, 32 / 4 heads, head_dim
     256: sampled rows against the oracle."""
