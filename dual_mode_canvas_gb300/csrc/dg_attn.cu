@@ -146,7 +146,7 @@ bool rotate_kv_order() {
 // Persistent grid: one CTA per SM (DG_ATTN_NUM_CTAS caps the number of CTAs,
 // for tests of the split-KV path).
 int num_ctas_for(const DeviceInfo& di) {
-  int n = di.num_sms;
+  int n = std::min(di.num_sms, kMaxCtas);
   if (const char* e = std::getenv("DG_ATTN_NUM_CTAS")) {
     const int v = std::max(1, std::atoi(e));
     if (v < n) n = v;
@@ -159,6 +159,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 struct Layout {
   size_t hdr, seq_tile, seq_kv, tiles, unit_begin, part_lse, part_o, total;
   int max_tiles;
+  bool local;  // at most kLocalMaxTiles tiles: one copy of the tile tables per CTA
 };
 
 Layout make_layout(int B, int total_q, int Hq, int Hkv, int D, int num_sms) {
@@ -167,12 +168,16 @@ Layout make_layout(int B, int total_q, int Hq, int Hkv, int D, int num_sms) {
   Layout l;
   const int64_t mt = (static_cast<int64_t>(total_q) + TT - 1) / TT + B;
   l.max_tiles = static_cast<int>(static_cast<int64_t>(Hkv) * mt);
+  // small batches: every CTA of the attention grid builds the work list into
+  // its own copy of the tables
+  l.local = l.max_tiles <= kLocalMaxTiles;
+  const size_t copies = l.local ? static_cast<size_t>(num_sms) : 1;
   size_t off = 0;
   l.hdr = off;        off = align256(off + sizeof(WorkHeader));
   l.seq_tile = off;   off = align256(off + sizeof(int64_t) * (B + 1));
   l.seq_kv = off;     off = align256(off + sizeof(int64_t) * (B + 1));
-  l.tiles = off;      off = align256(off + sizeof(TileDesc) * static_cast<size_t>(l.max_tiles));
-  l.unit_begin = off; off = align256(off + sizeof(int64_t) * (static_cast<size_t>(l.max_tiles) + 1));
+  l.tiles = off;      off = align256(off + sizeof(TileDesc) * static_cast<size_t>(l.max_tiles) * copies);
+  l.unit_begin = off; off = align256(off + sizeof(int64_t) * (static_cast<size_t>(l.max_tiles) + 1) * copies);
   l.part_lse = off;   off = align256(off + sizeof(float) * 2 * static_cast<size_t>(num_sms) * kRows);
   l.part_o = off;     off = align256(off + sizeof(float) * 2 * static_cast<size_t>(num_sms) * kRows * D);
   l.total = off;
@@ -419,10 +424,38 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   }
   const int num_ctas = num_ctas_for(*di);
   p.num_slots = 2 * num_ctas;
-  build_worklist_kernel<<<1 + append_ctas, 1024, 0, stream>>>(
-      cu_q, ctx_len, mode, num_seqs, total_q, pg ? INT32_MAX : total_kv, num_kv_heads, TT, BN,
-      window, lay.max_tiles, num_ctas, rotate_kv_order() ? 1 : 0, p.seg_weight, p.ws, pa, p.status);
-  if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+  // Small batches with contiguous K/V have no work-list grid: every CTA of
+  // the attention grid builds the list for itself (measured: the work-list
+  // grid's launch and run cost a denoise step ~5 us on the critical path).
+  // DG_ATTN_FUSED_WL=0 keeps the separate grid.
+  const char* fwl_env = std::getenv("DG_ATTN_FUSED_WL");
+  p.fused_wl = (!pg && lay.local && !(fwl_env && std::strcmp(fwl_env, "0") == 0)) ? 1 : 0;
+  p.cu_q = cu_q;
+  p.ctx_len = ctx_len;
+  p.mode = mode;
+  p.B = num_seqs;
+  p.max_tiles = lay.max_tiles;
+  p.tiles_stride = p.fused_wl ? lay.max_tiles : 0;
+  p.ub_stride = p.fused_wl ? lay.max_tiles + 1 : 0;
+  p.rotate = rotate_kv_order() ? 1 : 0;
+  p.kv_total = pg ? 0 : total_kv;
+  // a programmatic dependent of the stream's previous kernel (it waits for
+  // that grid before reading anything), so in a loop of calls its launch
+  // overlaps the previous call's merge
+  cudaLaunchConfig_t wcfg = {};
+  wcfg.gridDim = dim3(1 + append_ctas);
+  wcfg.blockDim = dim3(1024);
+  wcfg.stream = stream;
+  cudaLaunchAttribute wattr[1];
+  wattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  wattr[0].val.programmaticStreamSerializationAllowed = 1;
+  wcfg.attrs = wattr;
+  wcfg.numAttrs = 1;
+  if (!p.fused_wl &&
+      cudaLaunchKernelEx(&wcfg, build_worklist_kernel, cu_q, ctx_len, mode, num_seqs, total_q,
+                         pg ? INT32_MAX : total_kv, num_kv_heads, TT, BN, window, lay.max_tiles, num_ctas,
+                         p.rotate, p.seg_weight, p.ws, pa, p.status) != cudaSuccess)
+    return DG_ERR_CUDA;
   cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
   if (f8) {
     if (head_dim == 128) return launch<128, true>(mk, mv, p, num_ctas, lay.max_tiles, stream, e0, e1);

@@ -6,11 +6,15 @@
 //                          range is the union of the rows' windows (causal:
 //                          keys <= i, bidirectional: the whole sequence, both
 //                          narrowed to [i-W, i+W] on sliding-window layers).
+//                          Batches of at most kLocalMaxTiles tiles with
+//                          contiguous K/V skip this grid: every CTA of the
+//                          attention grid builds the same list for itself.
 //   fwd_kernel<D,BN,NK,NV,F8,NS,QS> persistent, one CTA per SM.  The (tile,
 //                          KV-tile) work units are split over the CTAs by
-//                          weight; every CTA TMA-loads the K/V tiles it
-//                          consumes from this GPU's memory into its own shared
-//                          memory.  A tile cut between CTAs leaves fp32
+//                          weight; each CTA keeps the tiles of its range in a
+//                          shared-memory window and TMA-loads the K/V tiles
+//                          it consumes from this GPU's memory into its own
+//                          shared memory.  A tile cut between CTAs leaves fp32
 //                          partials + LSE.
 //                          Warp roles: warps 4 and 6 issue TMA loads (K ring,
 //                          V ring; warp 7 shares the K boxes of tiles of small
@@ -91,6 +95,29 @@ __device__ __forceinline__ int kv_tile(const TileDesc& td, int j) {
   return td.kt_first + x;
 }
 
+// The work list as one CTA of the attention kernel reads it: the descriptors
+// and unit starts of a window of up to kWinTiles tiles, from the tile holding
+// the CTA's first unit, in shared memory; tiles past the window from the
+// global tables.  (A CTA's unit range spans one to three tiles in the
+// configured workloads.)
+constexpr int kWinTiles = 16;
+struct WorkView {
+  const TileDesc* g_tiles;  // global tile table (this CTA's copy, or the work-list grid's)
+  const int64_t* g_ub;      // global unit starts, [num_tiles + 1]
+  int t0, n;                // the window holds tiles t0 .. t0 + n - 1
+  int scratch[2];
+  TileDesc s_tiles[kWinTiles];
+  int64_t s_ub[kWinTiles + 1];  // unit starts of tiles t0 .. t0 + n
+  __device__ __forceinline__ int64_t ub(int t) const {
+    const unsigned i = static_cast<unsigned>(t - t0);
+    return i <= static_cast<unsigned>(n) ? s_ub[i] : g_ub[t];
+  }
+  __device__ __forceinline__ TileDesc tile(int t) const {
+    const unsigned i = static_cast<unsigned>(t - t0);
+    return i < static_cast<unsigned>(n) ? s_tiles[i] : g_tiles[t];
+  }
+};
+
 struct WorkHeader {
   int32_t num_tiles;  // query tiles
   int32_t error;
@@ -143,6 +170,18 @@ struct FwdParams {
   // of this (per-CTA) KV tile past the tensor, so its bounds check fails
   // (tests of the check; the load it guards is skipped)
   int debug_bad_kv_row;
+  // 1: no work-list grid; every CTA of the attention grid builds the work
+  // list itself from the metadata below (contiguous K/V, at most
+  // kLocalMaxTiles tiles).  CTA c keeps its copy of the tables at ws.tiles +
+  // c * tiles_stride and ws.unit_begin + c * ub_stride; CTA 0's copy, at the
+  // base, is the one the split-KV merge reads.
+  int fused_wl;
+  int tiles_stride, ub_stride;  // max_tiles and max_tiles + 1 with fused_wl, else 0
+  const int32_t* cu_q;
+  const int32_t* ctx_len;
+  const uint8_t* mode;
+  int B, max_tiles, rotate;
+  int64_t kv_total;  // K/V rows of the contiguous layout
   float scale, scale_log2;  // softmax scale (times the q and k scales for e4m3 inputs)
   float v_scale;            // e4m3 inputs: the v scale, applied in the epilogue (1 for bf16)
 };
@@ -301,19 +340,112 @@ __device__ __forceinline__ int64_t cta_unit_begin(int c, int64_t U, int P) {
   return static_cast<int64_t>(c) * U / P;
 }
 
-// CTA whose unit range contains unit u (ranges are [begin(c), begin(c+1))).
-__device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int P) {
-  int c = static_cast<int>((u * P) / U);
-  if (c > P - 1) c = P - 1;
-  while (c + 1 < P && cta_unit_begin(c + 1, U, P) <= u) ++c;
-  while (c > 0 && cta_unit_begin(c, U, P) > u) --c;
-  return c;
-}
-
 // ------------------------------------------------------ work-list builder
 // Per-sequence values of the builder live in shared memory for batches of up
 // to this many sequences (larger batches read them back from the workspace).
 constexpr int kWlSmemSeqs = 1024;
+// Batches of at most this many query tiles (with contiguous K/V) have no
+// work-list grid: each CTA of the attention grid builds the list itself.
+constexpr int kLocalMaxTiles = 256;
+// CTAs of the attention grid at most (the host caps the grid).
+constexpr int kMaxCtas = 1024;
+
+// Per-sequence values a tile descriptor is made from: first query row
+// (q0[B] = total_q), cached tokens, mode, tiles and K/V rows before the
+// sequence (shared memory or workspace).
+struct SeqTables {
+  const int32_t* q0;
+  const int32_t* ctx;
+  const uint8_t* mode;
+  const int64_t* toff;
+  const int64_t* kvoff;
+};
+
+// Descriptor of query tile `tile` (KV range and geometry; no split fields).
+// Tiles run sequence by sequence, KV head by KV head, TT tokens each.
+__device__ TileDesc make_tile_desc(int tile, const SeqTables& st, int B, int TT, int BN, int window,
+                                   bool paged, int bt_stride) {
+  // sequence owning this tile: largest s with tiles-before(s) <= tile
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (st.toff[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  const int s = lo;
+  const int q0 = st.q0[s];
+  const int n = st.q0[s + 1] - q0;
+  const int c = st.ctx[s];
+  const int L = c + n;
+  const bool causal = st.mode[s] == 0;
+  const int m_tiles = (n + TT - 1) / TT;
+  const int local = tile - static_cast<int>(st.toff[s]);
+  const int kvh = local / m_tiles;
+  const int mt = local - kvh * m_tiles;
+  const int t0 = mt * TT;
+  const int pos_first = c + t0;
+  const int i_max = c + min(n, t0 + TT) - 1;
+  const int kv_lo = window < 0 ? 0 : max(0, pos_first - window);
+  const int kv_hi = causal ? i_max : (window < 0 ? L - 1 : min(L - 1, i_max + window));
+  TileDesc td;
+  td.q_row0 = q0 + t0;
+  td.n_tok = min(TT, n - t0);
+  td.kv_row0 = paged ? s * bt_stride : static_cast<int>(st.kvoff[s]);
+  td.pos0 = pos_first;
+  td.L = L;
+  td.kt_first = kv_lo / BN;
+  td.kvh = kvh;
+  td.causal = causal ? 1 : 0;
+  td.kt_count = kv_hi / BN - kv_lo / BN + 1;
+  td.kt_rot = 0;
+  td.comb_cta = 0;
+  td.comb_n = 0;
+  td.comb_slot0 = 0;
+  td.pad_ = 0;
+  return td;
+}
+
+// Largest CTA c < P whose unit range starts at or before unit u, from the
+// table of range starts cbeg[0 .. P] (cbeg[c] = cta_unit_begin(c, U, P)).
+__device__ __forceinline__ int cta_of_unit_tab(int64_t u, const int64_t* cbeg, int P) {
+  int lo = 0, hi = P - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cbeg[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Fills cbeg[0 .. P] (shared memory); every thread of the block calls it.
+__device__ __forceinline__ void fill_cta_starts(int64_t* cbeg, int64_t U, int P) {
+  for (int c = threadIdx.x; c <= P; c += blockDim.x) cbeg[c] = cta_unit_begin(c, U, P);
+  __syncthreads();
+}
+
+// The split fields of a tile whose units start at ub (its KV tiles at
+// ub + seg_weight), given the starts cbeg[0 .. P] of the P CTA ranges (P = 0:
+// no units): the CTAs holding its KV tiles, the partial slot of the first,
+// and the KV visiting offset.  (A table lookup instead of the 64-bit divisions
+// of cta_of_unit: those put ~2 us on the critical path of every call.)
+__device__ void split_tile_desc(TileDesc& td, int64_t ub, int seg_weight, const int64_t* cbeg, int P,
+                                bool rotate) {
+  const int64_t r0 = ub + seg_weight, n = td.kt_count;
+  if (P <= 0) return;
+  const int c_lo = cta_of_unit_tab(r0, cbeg, P), c_hi = cta_of_unit_tab(r0 + n - 1, cbeg, P);
+  td.comb_cta = c_lo;
+  td.comb_n = c_hi - c_lo + 1;
+  td.comb_slot0 = cbeg[c_lo] >= ub ? 2 * c_lo : 2 * c_lo + 1;
+  // KV visiting order.  The CTAs' unit ranges are contiguous and equally
+  // long (U / P units), so the CTAs sharing one query tile start at KV-tile
+  // offsets a multiple of U / P apart.  Rotating each tile's KV tiles so
+  // that the CTA holding its first KV tile reaches that KV tile at "time"
+  // (units since the launch) equal to the KV tile's index gives every CTA
+  // of every query tile a phase that is a multiple of U / P: the query
+  // tiles of one (sequence, KV head) with the same KV range then stream the
+  // same KV tiles at about the same time, and the later readers find them
+  // in L2.  The order of the KV tiles does not change the result beyond
+  // fp32 rounding.
+  if (rotate && n > 1 && P > 1) td.kt_rot = static_cast<int>((r0 - cbeg[c_lo]) % n);
+}
 
 // CTA 0 builds the work list; with a paged cache, CTAs 1.. append the new K/V.
 // One read of the metadata, scans in registers and shared memory, one write
@@ -327,6 +459,11 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
   // the attention kernel is launched as a programmatic dependent: its CTAs
   // become resident while this grid runs and wait for it to finish
   griddep_launch_dependents();
+  // this grid is itself a programmatic dependent of the stream's previous
+  // kernel (the last call's split-KV merge, in a loop of calls): it becomes
+  // resident while that grid drains, and reads or writes nothing before it
+  // has finished
+  griddep_wait();
   if (blockIdx.x > 0) {
     append_rows(cu_q, ctx_len, B, total_q, pg, status);
     return;
@@ -337,6 +474,7 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
   __shared__ uint8_t s_mode[kWlSmemSeqs];
   __shared__ int64_t s_toff[kWlSmemSeqs + 1];  // tiles before each sequence
   __shared__ int64_t s_kvoff[kWlSmemSeqs];     // K/V rows before each sequence
+  __shared__ int64_t s_cbeg[kMaxCtas + 1];     // start unit of each CTA range
   const int tid = threadIdx.x;
   const bool paged = pg.block_table != nullptr;
   const bool small = B <= kWlSmemSeqs;
@@ -417,76 +555,23 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
   const int num_tiles = static_cast<int>(carry_t);
   const int per = (num_tiles + 1023) / 1024;
   const int t_begin = min(num_tiles, tid * per), t_end = min(num_tiles, t_begin + per);
-  auto make_tile = [&](int tile) {
-    // sequence owning this tile: largest s with tiles-before(s) <= tile
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if ((small ? s_toff[mid] : ws.seq_tile_off[mid]) <= tile) lo = mid; else hi = mid - 1;
-    }
-    const int s = lo;
-    const int q0 = q0_of(s);
-    const int n = q0_of(s + 1) - q0;
-    const int c = ctx_of(s);
-    const int L = c + n;
-    const bool causal = (small ? s_mode[s] : mode[s]) == 0;
-    const int m_tiles = (n + TT - 1) / TT;
-    const int local = tile - static_cast<int>(small ? s_toff[s] : ws.seq_tile_off[s]);
-    const int kvh = local / m_tiles;
-    const int mt = local - kvh * m_tiles;
-    const int t0 = mt * TT;
-    const int pos_first = c + t0;
-    const int i_max = c + min(n, t0 + TT) - 1;
-    const int kv_lo = window < 0 ? 0 : max(0, pos_first - window);
-    const int kv_hi = causal ? i_max : (window < 0 ? L - 1 : min(L - 1, i_max + window));
-    TileDesc td;
-    td.q_row0 = q0 + t0;
-    td.n_tok = min(TT, n - t0);
-    td.kv_row0 = paged ? s * pg.bt_stride : static_cast<int>(small ? s_kvoff[s] : ws.seq_kv_off[s]);
-    td.pos0 = pos_first;
-    td.L = L;
-    td.kt_first = kv_lo / BN;
-    td.kvh = kvh;
-    td.causal = causal ? 1 : 0;
-    td.kt_count = kv_hi / BN - kv_lo / BN + 1;
-    td.kt_rot = 0;
-    td.comb_cta = 0;
-    td.comb_n = 0;
-    td.comb_slot0 = 0;
-    td.pad_ = 0;
-    return td;
-  };
+  const SeqTables st{small ? s_q0 : cu_q, small ? s_ctx : ctx_len, small ? s_mode : mode,
+                     small ? s_toff : ws.seq_tile_off, small ? s_kvoff : ws.seq_kv_off};
+  auto make_tile = [&](int tile) { return make_tile_desc(tile, st, B, TT, BN, window, paged, pg.bt_stride); };
   // pass 1: the units of this thread's tiles, scanned over the block
   int64_t mine = 0;
   for (int t = t_begin; t < t_end; ++t) mine += seg_weight + make_tile(t).kt_count;
   int64_t U;
   int64_t ub = block_scan_1024(mine, &U);
   const int P = active_ctas(num_ctas, U);
+  fill_cta_starts(s_cbeg, U, P);
   // pass 2: the finished descriptors, written once
   for (int t = t_begin; t < t_end; ++t) {
     TileDesc td = make_tile(t);
-    const int64_t r0 = ub + seg_weight, n = td.kt_count;
-    // CTAs holding KV tiles of this tile, and the partial slot of the first
-    if (U > 0) {
-      const int c_lo = cta_of_unit(r0, U, P), c_hi = cta_of_unit(r0 + n - 1, U, P);
-      td.comb_cta = c_lo;
-      td.comb_n = c_hi - c_lo + 1;
-      td.comb_slot0 = cta_unit_begin(c_lo, U, P) >= ub ? 2 * c_lo : 2 * c_lo + 1;
-      // KV visiting order.  The CTAs' unit ranges are contiguous and equally
-      // long (U / P units), so the CTAs sharing one query tile start at KV-tile
-      // offsets a multiple of U / P apart.  Rotating each tile's KV tiles so
-      // that the CTA holding its first KV tile reaches that KV tile at "time"
-      // (units since the launch) equal to the KV tile's index gives every CTA
-      // of every query tile a phase that is a multiple of U / P: the query
-      // tiles of one (sequence, KV head) with the same KV range then stream the
-      // same KV tiles at about the same time, and the later readers find them
-      // in L2.  The order of the KV tiles does not change the result beyond
-      // fp32 rounding.
-      if (rotate && n > 1 && P > 1) td.kt_rot = static_cast<int>((r0 - cta_unit_begin(c_lo, U, P)) % n);
-    }
+    split_tile_desc(td, ub, seg_weight, s_cbeg, P, rotate != 0);
     ws.tiles[t] = td;
     ws.unit_begin[t] = ub;
-    ub += seg_weight + n;
+    ub += seg_weight + td.kt_count;
   }
   if (tid == 0) {
     ws.unit_begin[num_tiles] = U;
@@ -496,14 +581,219 @@ build_worklist_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restric
   }
 }
 
-// Tile containing unit u: largest t with unit_begin[t] <= u.
-__device__ __forceinline__ int tile_of_unit(const int64_t* ub, int num_tiles, int64_t u) {
-  int lo = 0, hi = num_tiles - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (ub[mid] <= u) lo = mid; else hi = mid - 1;
+// Exclusive scan of one value per thread over the block (a multiple of 32
+// threads, at most 1024); *total receives the block's sum.  wsum: 33 words of
+// shared scratch.  Every thread of the block must call it.
+__device__ int64_t block_scan_excl(int64_t x, int64_t* total, int64_t* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  int64_t incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  return lo;
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int64_t w = lane < nw ? wsum[lane] : 0;
+    int64_t wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < nw) wsum[lane] = wi - w;
+    if (lane == 31) wsum[32] = wi;
+  }
+  __syncthreads();
+  const int64_t r = wsum[warp] + incl - x;
+  *total = wsum[32];
+  __syncthreads();  // the shared words are reused by the next call
+  return r;
+}
+
+// Bytes of shared scratch build_worklist_cta uses.
+constexpr int kLocalWlScratch = 40 * 8 + (kMaxCtas + 1) * 8 + 2 * (kLocalMaxTiles + 1) * 8 +
+                                2 * (kLocalMaxTiles + 1) * 4 + (kLocalMaxTiles + 1);
+
+// This CTA's unit range [u_beg, u_end) of U units over the active CTAs (a CTA
+// past them, or a call without work, has an empty range).
+__device__ __forceinline__ void cta_range(int num_tiles, int64_t U, int64_t& u_beg, int64_t& u_end) {
+  const int cta = static_cast<int>(blockIdx.x);
+  const int P = U > 0 ? active_ctas(static_cast<int>(gridDim.x), U) : 1;
+  const bool active = num_tiles > 0 && U > 0 && cta < P;
+  u_beg = active ? cta_unit_begin(cta, U, P) : 0;
+  u_end = active ? cta_unit_begin(cta + 1, U, P) : 0;
+}
+
+// The work list of one call, built by a CTA of the attention grid for itself
+// (every CTA builds the same list): the checks, tiles, unit starts, visiting
+// offsets and merge contributors of build_worklist_kernel, from the same
+// helpers, written to this CTA's copy of the tile table and unit starts (CTA
+// 0 also writes the header) and, for the tiles from the one holding this
+// CTA's first unit on, to its shared-memory window.  Contiguous K/V and at
+// most kLocalMaxTiles tiles.  scratch: kLocalWlScratch bytes of shared
+// memory.  Every thread of the block calls it; it returns the tile and unit
+// counts (both 0 for invalid metadata, which it records as
+// DG_ERR_INVALID_ARG).  Kept out of line: inlined, its registers spilled the
+// attention kernel's e4m3 shapes.
+struct WlCounts {
+  int64_t units;
+  int num_tiles;
+};
+__device__ __noinline__ WlCounts build_worklist_cta(const FwdParams& p, int BN, TileDesc* tiles, int64_t* ub_out,
+                                                    uint8_t* scratch, WorkView* wv) {
+  constexpr int S = kLocalMaxTiles + 1;
+  int64_t* wsum = reinterpret_cast<int64_t*>(scratch);  // 33 used
+  int64_t* s_cbeg = wsum + 40;                          // start unit of each CTA range
+  int64_t* s_toff = s_cbeg + kMaxCtas + 1;              // tiles before each sequence
+  int64_t* s_kvoff = s_toff + S;                        // K/V rows before each sequence
+  int32_t* s_q0 = reinterpret_cast<int32_t*>(s_kvoff + S);
+  int32_t* s_ctx = s_q0 + S;
+  uint8_t* s_mode = reinterpret_cast<uint8_t*>(s_ctx + S);
+  const int tid = threadIdx.x, nthr = static_cast<int>(blockDim.x);
+  const int B = p.B;
+  // ---- sequences: tiles and K/V rows (B <= kLocalMaxTiles), every load of
+  // the metadata in one round trip
+  int bad = 0;
+  int64_t carry_t = 0, carry_kv = 0;
+  for (int base = 0; base < B; base += nthr) {
+    const int s = base + tid;
+    int64_t nt = 0, nkv = 0;
+    if (s < B) {
+      const int q0 = p.cu_q[s], q1 = p.cu_q[s + 1], c = p.ctx_len[s], md = p.mode[s];
+      const int n = q1 - q0;
+      if (n < 0 || c < 0 || md > 1 || (s == 0 && q0 != 0) || (s == B - 1 && q1 != p.total_q)) bad = 1;
+      const int64_t nn = n < 0 ? 0 : n;
+      nt = static_cast<int64_t>(p.Hkv) * ((nn + p.TT - 1) / p.TT);
+      nkv = static_cast<int64_t>(c < 0 ? 0 : c) + nn;
+      s_q0[s] = q0;
+      s_ctx[s] = c;
+      s_mode[s] = static_cast<uint8_t>(md);
+    }
+    int64_t sum_t, sum_kv;
+    const int64_t et = block_scan_excl(nt, &sum_t, wsum);
+    const int64_t ekv = block_scan_excl(nkv, &sum_kv, wsum);
+    if (s < B) {
+      s_toff[s] = carry_t + et;
+      s_kvoff[s] = carry_kv + ekv;
+    }
+    carry_t += sum_t;
+    carry_kv += sum_kv;
+  }
+  if (tid == 0) {
+    s_toff[B] = carry_t;
+    s_q0[B] = p.total_q;
+  }
+  if (carry_t > p.max_tiles || carry_kv > p.kv_total) bad = 1;
+  if (__syncthreads_or(bad)) {
+    if (blockIdx.x == 0 && tid == 0) {
+      p.ws.hdr->num_tiles = 0;
+      p.ws.hdr->total_units = 0;
+      p.ws.hdr->error = kErrInvalid;
+      record_error(p.status, kErrInvalid);
+    }
+    if (tid == 0) {
+      wv->g_tiles = tiles;
+      wv->g_ub = ub_out;
+      wv->t0 = 0;
+      wv->n = 0;
+    }
+    __syncthreads();
+    return WlCounts{0, 0};
+  }
+  // ---- tiles: thread tid owns the consecutive tiles [t_begin, t_end)
+  const int num_tiles = static_cast<int>(carry_t);
+  const int per = (num_tiles + nthr - 1) / nthr;
+  const int t_begin = min(num_tiles, tid * per), t_end = min(num_tiles, t_begin + per);
+  const SeqTables st{s_q0, s_ctx, s_mode, s_toff, s_kvoff};
+  int64_t mine = 0;
+  for (int t = t_begin; t < t_end; ++t)
+    mine += p.seg_weight + make_tile_desc(t, st, B, p.TT, BN, p.window, false, 0).kt_count;
+  int64_t U;
+  const int64_t ub0 = block_scan_excl(mine, &U, wsum);
+  const int P = active_ctas(static_cast<int>(gridDim.x), U);
+  int64_t u_beg, u_end;
+  cta_range(num_tiles, U, u_beg, u_end);
+  // the tile holding this CTA's first unit starts the window (found by the
+  // one thread whose tiles hold that unit)
+  if (tid == 0) wv->scratch[0] = 0;
+  fill_cta_starts(s_cbeg, U, P);
+  if (u_beg < u_end && ub0 <= u_beg && u_beg < ub0 + mine) {
+    int64_t ub = ub0;
+    for (int t = t_begin; t < t_end; ++t) {
+      const int64_t len = p.seg_weight + make_tile_desc(t, st, B, p.TT, BN, p.window, false, 0).kt_count;
+      if (ub <= u_beg && u_beg < ub + len) wv->scratch[0] = t;
+      ub += len;
+    }
+  }
+  __syncthreads();
+  const int t0 = wv->scratch[0];
+  const int nwin = u_beg < u_end ? min(kWinTiles, num_tiles - t0) : 0;
+  int64_t ub = ub0;
+  for (int t = t_begin; t < t_end; ++t) {
+    TileDesc td = make_tile_desc(t, st, B, p.TT, BN, p.window, false, 0);
+    split_tile_desc(td, ub, p.seg_weight, s_cbeg, P, p.rotate != 0);
+    tiles[t] = td;
+    ub_out[t] = ub;
+    const int i = t - t0;
+    if (i >= 0 && i < nwin) wv->s_tiles[i] = td;
+    if (i >= 0 && i <= nwin) wv->s_ub[i] = ub;
+    ub += p.seg_weight + td.kt_count;
+  }
+  if (tid == 0) {
+    ub_out[num_tiles] = U;
+    if (t0 + nwin == num_tiles) wv->s_ub[nwin] = U;
+    wv->g_tiles = tiles;
+    wv->g_ub = ub_out;
+    wv->t0 = t0;
+    wv->n = nwin;
+    if (blockIdx.x == 0) {
+      p.ws.hdr->num_tiles = num_tiles;
+      p.ws.hdr->total_units = U;
+      p.ws.hdr->error = 0;
+    }
+  }
+  __syncthreads();  // the tables and the window are complete for every thread of the CTA
+  return WlCounts{U, num_tiles};
+}
+
+// The window of a work list the work-list grid wrote: the tile holding this
+// CTA's first unit is found by a parallel search of the unit starts (rounds
+// of one load per thread, each narrowing the range by the block size), then
+// the window's descriptors are copied.  Every thread of the block calls it.
+__device__ __noinline__ void load_window(const TileDesc* tiles, const int64_t* ubg, int num_tiles, int64_t U,
+                                         WorkView* wv) {
+  const int tid = threadIdx.x, nthr = static_cast<int>(blockDim.x);
+  int64_t u_beg, u_end;
+  cta_range(num_tiles, U, u_beg, u_end);
+  int lo = 0, hi = num_tiles;  // the tile holding u_beg is in [lo, hi)
+  while (u_beg < u_end && hi - lo > 1) {
+    const int stride = (hi - lo + nthr - 1) / nthr;
+    if (tid == 0) wv->scratch[0] = lo;
+    __syncthreads();
+    const int a = lo + tid * stride;
+    if (a < hi) {
+      const int b = min(hi, a + stride);
+      if (ubg[a] <= u_beg && u_beg < ubg[b]) wv->scratch[0] = a;
+    }
+    __syncthreads();
+    lo = wv->scratch[0];
+    hi = min(hi, lo + stride);
+    __syncthreads();
+  }
+  const int t0 = lo;
+  const int nwin = u_beg < u_end ? min(kWinTiles, num_tiles - t0) : 0;
+  if (tid < nwin) wv->s_tiles[tid] = tiles[t0 + tid];
+  if (tid <= nwin && u_beg < u_end) wv->s_ub[tid] = ubg[t0 + tid];
+  if (tid == 0) {
+    wv->g_tiles = tiles;
+    wv->g_ub = ubg;
+    wv->t0 = t0;
+    wv->n = nwin;
+  }
+  __syncthreads();
 }
 
 struct Seg {
@@ -516,23 +806,26 @@ struct Seg {
 // Walks the segments of one CTA's unit range; every role walks the same
 // list.  A query tile spans units [ub[t], ub[t+1]); its KV tiles are the units
 // from ub[t] + seg_w on, so a range that only touches a tile's first seg_w
-// units yields no segment of it.
+// units yields no segment of it.  The walk goes tile by tile from the tile
+// holding the range's first unit (every tile has at least one KV tile, so the
+// unit starts strictly increase).
 struct SegIter {
-  const int64_t* ub;
-  int num_tiles;
+  const WorkView* wv;
+  int t;  // the tile holding unit u
   int64_t u, u_end;
   int cta;
   bool first;
   int seg_w;
   __device__ bool next(Seg& sg) {
     while (u < u_end) {
-      const int t = tile_of_unit(ub, num_tiles, u);
-      const int64_t r0 = ub[t] + seg_w, t1 = ub[t + 1];
+      const int tt = t;
+      const int64_t r0 = wv->ub(tt) + seg_w, t1 = wv->ub(tt + 1);
       const int64_t b = u > r0 ? u : r0;
       const int64_t e = u_end < t1 ? u_end : t1;
       u = e;
+      if (e == t1) ++t;
       if (b >= e) continue;
-      sg.tile = t;
+      sg.tile = tt;
       sg.j0 = static_cast<int>(b - r0);
       sg.j1 = static_cast<int>(e - r0);
       sg.whole = (b == r0 && e == t1) ? 1 : 0;
@@ -641,7 +934,8 @@ struct FwdCfg {
                        B_O_FREE = B_V_EMPTY + NV,
                        B_DRAIN = B_O_FREE + 1, NUM_BARS = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int OFF_WORK = OFF_MISC + 16;  // the CTA's WorkView
+  static constexpr int SMEM_USED = OFF_WORK + static_cast<int>(sizeof(WorkView));
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
   // TMEM columns: O (fp32, D), NS S buffers (fp32, BN; P overwrites the first
   // BN / PER_WORD columns, packed), Q (packed, D / PER_WORD; not with QS).
@@ -744,10 +1038,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 
   griddep_wait();
   griddep_launch_dependents();
-  const WorkHeader* hdr = p.ws.hdr;
-  const int num_tiles = hdr->num_tiles;
-  const int64_t U = hdr->total_units;
   const int cta = static_cast<int>(blockIdx.x);
+  // The work list: built here by every CTA for itself (no work-list grid), or
+  // read from the tables the work-list grid wrote; either way the CTA's first
+  // tiles land in its shared-memory window.
+  WorkView* wv = reinterpret_cast<WorkView*>(sptr + Cf::OFF_WORK);
+  int num_tiles;
+  int64_t U;
+  if (p.fused_wl) {
+    static_assert(NK * Cf::KV_BYTES >= kLocalWlScratch, "work-list scratch in the K ring");
+    const WlCounts wc = build_worklist_cta(p, BN, p.ws.tiles + static_cast<size_t>(cta) * p.tiles_stride,
+                                           p.ws.unit_begin + static_cast<size_t>(cta) * p.ub_stride,
+                                           sptr + Cf::OFF_K, wv);
+    num_tiles = wc.num_tiles;
+    U = wc.units;
+    // the scratch was the K ring, which the TMA unit (async proxy) writes next
+    fence_proxy_async_smem();
+    __syncthreads();
+  } else {
+    num_tiles = p.ws.hdr->num_tiles;
+    U = p.ws.hdr->total_units;
+    load_window(p.ws.tiles, p.ws.unit_begin, num_tiles, U, wv);
+  }
   const int P = U > 0 ? active_ctas(static_cast<int>(gridDim.x), U) : 1;
   // a CTA without work (no tiles, or more CTAs than units) walks an empty
   // range: every role finds nothing to do and the CTA frees its TMEM
@@ -755,7 +1067,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   const int64_t u_beg = active ? cta_unit_begin(cta, U, P) : 0;
   const int64_t u_end = active ? cta_unit_begin(cta + 1, U, P) : 0;
 
-  SegIter it{p.ws.unit_begin, num_tiles, u_beg, u_end, cta, true, p.seg_weight};
+  SegIter it{wv, wv->t0, u_beg, u_end, cta, true, p.seg_weight};
   const int G = p.G, TT = p.TT;
 
   if (warp == kTmaWarp || warp == kVLoadWarp || (warp == kTmaWarp2 && p.k_split)) {
@@ -795,20 +1107,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     bool ok = true;
     Seg sg;
     while (ok && it.next(sg)) {
-      const TileDesc td = p.ws.tiles[sg.tile];
-      if (is_k && kw == 0) {
-        // the next segment's Q rows go to L2 while this segment streams, so
-        // the softmax warps load them at L2 latency at the segment switch
-        SegIter look = it;
-        Seg nx;
-        if (look.next(nx)) {
-          const TileDesc tn = p.ws.tiles[nx.tile];
-          for (int t = lane; t < tn.n_tok; t += 32)
-            prefetch_l2_bulk(static_cast<const uint8_t*>(p.q) +
-                                 (static_cast<size_t>(tn.q_row0 + t) * p.Hq + tn.kvh * G) * D * E::SIZE,
-                             static_cast<uint32_t>(G * D * E::SIZE));
-        }
-      }
+      const TileDesc td = wv->tile(sg.tile);
+      // the next segment's Q rows go to L2 while this segment streams, so the
+      // softmax warps load them at L2 latency at the segment switch; issued
+      // after this segment's first K tile (issuing the bulk prefetches first
+      // delayed a call's first K load by ~3 us)
+      bool q_prefetch = is_k && kw == 0;
       // positions past the sequence's last key read its last page (checked
       // by the work-list launch); the softmax masks them
       const int last_page = (td.L - 1) >> p.page_shift;
@@ -863,6 +1167,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           if (ok_box) {
             if (page_box) tma_load_4d(dst, map, full0 + 8u * stage, 0, td.kvh, row, 0);
             else tma_load_3d(dst, map, full0 + 8u * stage, bk * E::BLK, td.kvh, row);
+          }
+        }
+        if (q_prefetch) {
+          q_prefetch = false;
+          SegIter look = it;
+          Seg nx;
+          if (look.next(nx)) {
+            const TileDesc tn = wv->tile(nx.tile);
+            for (int t = lane; t < tn.n_tok; t += 32)
+              prefetch_l2_bulk(static_cast<const uint8_t*>(p.q) +
+                                   (static_cast<size_t>(tn.q_row0 + t) * p.Hq + tn.kvh * G) * D * E::SIZE,
+                               static_cast<uint32_t>(G * D * E::SIZE));
           }
         }
         issued_mask |= 1u << stage;
@@ -1037,7 +1353,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     Seg sg;
     bool have = it.next(sg);
     if (have) {
-      q_issue(p.ws.tiles[sg.tile]);
+      q_issue(wv->tile(sg.tile));
       q_commit();
     }
     // With head_dim 256 and Q in TMEM the register file has room to stage
@@ -1047,7 +1363,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     constexpr bool kStageQ = (D == 256) && !QS;
     bool q_loaded = true;  // the first segment's Q is already committed
     while (ok && have) {
-      const TileDesc td = p.ws.tiles[sg.tile];
+      const TileDesc td = wv->tile(sg.tile);
       if (!q_loaded) {
         q_issue(td);
         q_commit();
@@ -1194,7 +1510,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       Seg nx;
       SegIter look = it;
       const bool more = kStageQ && look.next(nx);
-      if (more) q_issue(p.ws.tiles[nx.tile]);
+      if (more) q_issue(wv->tile(nx.tile));
       const float inv_l = l_run > 0.f ? p.v_scale / l_run : 0.f;
       // l_run sums the probabilities scaled by 2^P_SHIFT
       const float lse_v = l_run > 0.f ? m_run * p.scale + logf(l_run) - E::P_SHIFT * 0.6931471805599453f
@@ -1263,21 +1579,28 @@ constexpr int kCombineWarps = 8;
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const FwdParams p) {
+  // the next call's first grid (work list, or attention) may become
+  // resident now: it waits for this grid before it reads or writes memory
+  griddep_launch_dependents();
   const int tile = blockIdx.x;
   const int G = p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * kCombineWarps + warp;
   if (r >= G * p.TT) return;
   const int t = r / G, gi = r - t * G;
-  // The tile table was complete before the attention grid released this
-  // grid, so it is read before the wait; only the partials wait for the
-  // attention grid.  Both loads issued together (the descriptor of a tile
-  // past num_tiles is stale but lies inside the workspace and is not used).
+  // A tile table written by the work-list grid was complete before the
+  // attention grid released this grid, so it is read before the wait and
+  // only the partials wait for the attention grid (both loads issued
+  // together; the descriptor of a tile past num_tiles is stale but lies
+  // inside the workspace and is not used).  A table the attention grid built
+  // itself is complete only once that grid has finished: read after the wait.
+  const bool early = !p.fused_wl;
+  if (!early) griddep_wait();
   const int num_tiles = p.ws.hdr->num_tiles;
   const TileDesc td = p.ws.tiles[tile];
   if (tile >= num_tiles || td.comb_n <= 1) return;  // no tile, or written directly by one CTA
   if (t >= td.n_tok) return;
-  griddep_wait();
+  if (early) griddep_wait();
   const int nc = td.comb_n;
   // partial slot of contributor i: the first CTA's is recorded, the others
   // hold the tile in their first segment
