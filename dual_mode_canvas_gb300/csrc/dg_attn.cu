@@ -429,7 +429,10 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   // grid's launch and run cost a denoise step ~5 us on the critical path).
   // DG_ATTN_FUSED_WL=0 keeps the separate grid.
   const char* fwl_env = std::getenv("DG_ATTN_FUSED_WL");
-  p.fused_wl = (!pg && lay.local && !(fwl_env && std::strcmp(fwl_env, "0") == 0)) ? 1 : 0;
+  // (not the e4m3 head_dim-128 shape, whose kernel reads the work-list grid's
+  // tables directly)
+  p.fused_wl = (!pg && lay.local && !(f8 && head_dim == 128) && !(fwl_env && std::strcmp(fwl_env, "0") == 0))
+                   ? 1 : 0;
   p.cu_q = cu_q;
   p.ctx_len = ctx_len;
   p.mode = mode;

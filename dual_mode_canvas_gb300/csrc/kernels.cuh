@@ -44,6 +44,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -642,7 +643,19 @@ struct WlCounts {
   int64_t units;
   int num_tiles;
 };
-__device__ __noinline__ WlCounts build_worklist_cta(const FwdParams& p, int BN, TileDesc* tiles, int64_t* ub_out,
+// The call's metadata and sizes the in-grid builder reads.  (Passed by value:
+// a reference to the kernel's parameter block made the e4m3 head_dim-128
+// kernel read its parameters from a local copy.)
+struct WlArgs {
+  const int32_t* cu_q;
+  const int32_t* ctx_len;
+  const uint8_t* mode;
+  WorkHeader* hdr;
+  int* status;
+  int64_t kv_total;
+  int B, total_q, Hkv, TT, window, seg_weight, max_tiles, rotate;
+};
+__device__ __noinline__ WlCounts build_worklist_cta(const WlArgs p, int BN, TileDesc* tiles, int64_t* ub_out,
                                                     uint8_t* scratch, WorkView* wv) {
   constexpr int S = kLocalMaxTiles + 1;
   int64_t* wsum = reinterpret_cast<int64_t*>(scratch);  // 33 used
@@ -689,9 +702,9 @@ __device__ __noinline__ WlCounts build_worklist_cta(const FwdParams& p, int BN, 
   if (carry_t > p.max_tiles || carry_kv > p.kv_total) bad = 1;
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && tid == 0) {
-      p.ws.hdr->num_tiles = 0;
-      p.ws.hdr->total_units = 0;
-      p.ws.hdr->error = kErrInvalid;
+      p.hdr->num_tiles = 0;
+      p.hdr->total_units = 0;
+      p.hdr->error = kErrInvalid;
       record_error(p.status, kErrInvalid);
     }
     if (tid == 0) {
@@ -750,9 +763,9 @@ __device__ __noinline__ WlCounts build_worklist_cta(const FwdParams& p, int BN, 
     wv->t0 = t0;
     wv->n = nwin;
     if (blockIdx.x == 0) {
-      p.ws.hdr->num_tiles = num_tiles;
-      p.ws.hdr->total_units = U;
-      p.ws.hdr->error = 0;
+      p.hdr->num_tiles = num_tiles;
+      p.hdr->total_units = U;
+      p.hdr->error = 0;
     }
   }
   __syncthreads();  // the tables and the window are complete for every thread of the CTA
@@ -826,6 +839,43 @@ struct SegIter {
       if (e == t1) ++t;
       if (b >= e) continue;
       sg.tile = tt;
+      sg.j0 = static_cast<int>(b - r0);
+      sg.j1 = static_cast<int>(e - r0);
+      sg.whole = (b == r0 && e == t1) ? 1 : 0;
+      sg.slot = first ? 2 * cta : 2 * cta + 1;
+      first = false;
+      return true;
+    }
+    return false;
+  }
+};
+
+// The same walk over the global unit starts (a binary search per segment),
+// for the kernel shape that reads the work-list grid's tables directly.
+__device__ __forceinline__ int tile_of_unit(const int64_t* ub, int num_tiles, int64_t u) {
+  int lo = 0, hi = num_tiles - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ub[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+struct SegIterG {
+  const int64_t* ub;
+  int num_tiles;
+  int64_t u, u_end;
+  int cta;
+  bool first;
+  int seg_w;
+  __device__ bool next(Seg& sg) {
+    while (u < u_end) {
+      const int t = tile_of_unit(ub, num_tiles, u);
+      const int64_t r0 = ub[t] + seg_w, t1 = ub[t + 1];
+      const int64_t b = u > r0 ? u : r0;
+      const int64_t e = u_end < t1 ? u_end : t1;
+      u = e;
+      if (b >= e) continue;
+      sg.tile = t;
       sg.j0 = static_cast<int>(b - r0);
       sg.j1 = static_cast<int>(e - r0);
       sg.whole = (b == r0 && e == t1) ? 1 : 0;
@@ -934,8 +984,7 @@ struct FwdCfg {
                        B_O_FREE = B_V_EMPTY + NV,
                        B_DRAIN = B_O_FREE + 1, NUM_BARS = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int OFF_WORK = OFF_MISC + 16;  // the CTA's WorkView
-  static constexpr int SMEM_USED = OFF_WORK + static_cast<int>(sizeof(WorkView));
+  static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
   // TMEM columns: O (fp32, D), NS S buffers (fp32, BN; P overwrites the first
   // BN / PER_WORD columns, packed), Q (packed, D / PER_WORD; not with QS).
@@ -957,7 +1006,8 @@ struct FwdCfg {
   static_assert(NV >= NS - 1, "O_DONE reuse");
   static_assert(OFF_Q % 1024 == 0, "the swizzled query tile starts on a 1024-byte boundary");
   static_assert(D + NS * BN + (QS ? 0 : D / E::PER_WORD) <= static_cast<int>(kTmemCols), "TMEM budget");
-  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  // (the kernel's WorkView is static shared memory, beside this dynamic part)
+  static_assert(SMEM_BYTES + sizeof(WorkView) <= 232448, "shared memory budget");
 };
 
 template <int D, int BN, int NK, int NV, bool F8 = false, int NS = 2, bool QS = false>
@@ -1042,12 +1092,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   // The work list: built here by every CTA for itself (no work-list grid), or
   // read from the tables the work-list grid wrote; either way the CTA's first
   // tiles land in its shared-memory window.
-  WorkView* wv = reinterpret_cast<WorkView*>(sptr + Cf::OFF_WORK);
+  // (static shared memory: its address is a constant, so the roles hold no
+  // register for it; measured against the window in the dynamic part, the
+  // denoise step 1.7 us shorter)
+  __shared__ WorkView wv_s;
+  WorkView* wv = &wv_s;
+  // The e4m3 head_dim-128 shape keeps the walk over the work-list grid's
+  // global tables (the host never builds its list in the grid): with the
+  // window and the in-grid build its kernel ran 3.7% slower on the max mix
+  // (0.722 vs 0.696 ms), a code-generation effect at its 255-register limit
+  // that no single part of the change accounted for.
+  constexpr bool kGlobalWalk = F8 && D == 128;
+  using Iter = std::conditional_t<kGlobalWalk, SegIterG, SegIter>;
   int num_tiles;
   int64_t U;
-  if (p.fused_wl) {
+  if constexpr (kGlobalWalk) {
+    num_tiles = p.ws.hdr->num_tiles;
+    U = p.ws.hdr->total_units;
+  } else if (p.fused_wl) {
     static_assert(NK * Cf::KV_BYTES >= kLocalWlScratch, "work-list scratch in the K ring");
-    const WlCounts wc = build_worklist_cta(p, BN, p.ws.tiles + static_cast<size_t>(cta) * p.tiles_stride,
+    const WlArgs wa{p.cu_q, p.ctx_len, p.mode, p.ws.hdr, p.status, p.kv_total, p.B, p.total_q, p.Hkv, p.TT,
+                    p.window, p.seg_weight, p.max_tiles, p.rotate};
+    const WlCounts wc = build_worklist_cta(wa, BN, p.ws.tiles + static_cast<size_t>(cta) * p.tiles_stride,
                                            p.ws.unit_begin + static_cast<size_t>(cta) * p.ub_stride,
                                            sptr + Cf::OFF_K, wv);
     num_tiles = wc.num_tiles;
@@ -1067,7 +1133,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   const int64_t u_beg = active ? cta_unit_begin(cta, U, P) : 0;
   const int64_t u_end = active ? cta_unit_begin(cta + 1, U, P) : 0;
 
-  SegIter it{wv, wv->t0, u_beg, u_end, cta, true, p.seg_weight};
+  Iter it = [&]() -> Iter {
+    if constexpr (kGlobalWalk) return SegIterG{p.ws.unit_begin, num_tiles, u_beg, u_end, cta, true, p.seg_weight};
+    else return SegIter{wv, wv->t0, u_beg, u_end, cta, true, p.seg_weight};
+  }();
+  auto tile_at = [&](int t) -> TileDesc {
+    if constexpr (kGlobalWalk) return p.ws.tiles[t];
+    else return wv->tile(t);
+  };
   const int G = p.G, TT = p.TT;
 
   if (warp == kTmaWarp || warp == kVLoadWarp || (warp == kTmaWarp2 && p.k_split)) {
@@ -1107,12 +1180,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     bool ok = true;
     Seg sg;
     while (ok && it.next(sg)) {
-      const TileDesc td = wv->tile(sg.tile);
-      // the next segment's Q rows go to L2 while this segment streams, so the
-      // softmax warps load them at L2 latency at the segment switch; issued
-      // after this segment's first K tile (issuing the bulk prefetches first
-      // delayed a call's first K load by ~3 us)
-      bool q_prefetch = is_k && kw == 0;
+      const TileDesc td = tile_at(sg.tile);
+      if (is_k && kw == 0) {
+        // the next segment's Q rows go to L2 while this segment streams, so
+        // the softmax warps load them at L2 latency at the segment switch
+        Iter look = it;
+        Seg nx;
+        if (look.next(nx)) {
+          const TileDesc tn = tile_at(nx.tile);
+          for (int t = lane; t < tn.n_tok; t += 32)
+            prefetch_l2_bulk(static_cast<const uint8_t*>(p.q) +
+                                 (static_cast<size_t>(tn.q_row0 + t) * p.Hq + tn.kvh * G) * D * E::SIZE,
+                             static_cast<uint32_t>(G * D * E::SIZE));
+        }
+      }
       // positions past the sequence's last key read its last page (checked
       // by the work-list launch); the softmax masks them
       const int last_page = (td.L - 1) >> p.page_shift;
@@ -1167,18 +1248,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
           if (ok_box) {
             if (page_box) tma_load_4d(dst, map, full0 + 8u * stage, 0, td.kvh, row, 0);
             else tma_load_3d(dst, map, full0 + 8u * stage, bk * E::BLK, td.kvh, row);
-          }
-        }
-        if (q_prefetch) {
-          q_prefetch = false;
-          SegIter look = it;
-          Seg nx;
-          if (look.next(nx)) {
-            const TileDesc tn = wv->tile(nx.tile);
-            for (int t = lane; t < tn.n_tok; t += 32)
-              prefetch_l2_bulk(static_cast<const uint8_t*>(p.q) +
-                                   (static_cast<size_t>(tn.q_row0 + t) * p.Hq + tn.kvh * G) * D * E::SIZE,
-                               static_cast<uint32_t>(G * D * E::SIZE));
           }
         }
         issued_mask |= 1u << stage;
@@ -1353,7 +1422,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     Seg sg;
     bool have = it.next(sg);
     if (have) {
-      q_issue(wv->tile(sg.tile));
+      q_issue(tile_at(sg.tile));
       q_commit();
     }
     // With head_dim 256 and Q in TMEM the register file has room to stage
@@ -1363,7 +1432,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     constexpr bool kStageQ = (D == 256) && !QS;
     bool q_loaded = true;  // the first segment's Q is already committed
     while (ok && have) {
-      const TileDesc td = wv->tile(sg.tile);
+      const TileDesc td = tile_at(sg.tile);
       if (!q_loaded) {
         q_issue(td);
         q_commit();
@@ -1508,9 +1577,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       }
       tc_fence_after();
       Seg nx;
-      SegIter look = it;
+      Iter look = it;
       const bool more = kStageQ && look.next(nx);
-      if (more) q_issue(wv->tile(nx.tile));
+      if (more) q_issue(tile_at(nx.tile));
       const float inv_l = l_run > 0.f ? p.v_scale / l_run : 0.f;
       // l_run sums the probabilities scaled by 2^P_SHIFT
       const float lse_v = l_run > 0.f ? m_run * p.scale + logf(l_run) - E::P_SHIFT * 0.6931471805599453f
