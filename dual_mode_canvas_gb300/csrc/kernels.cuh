@@ -12,9 +12,9 @@
 //   fwd_kernel<D,BN,NK,NV,F8,NS,QS> persistent, one CTA per SM.  The (tile,
 //                          KV-tile) work units are split over the CTAs by
 //                          weight; each CTA keeps the tiles of its range in a
-//                          shared-memory window and TMA-loads the K/V tiles
-//                          it consumes from this GPU's memory into its own
-//                          shared memory.  A tile cut between CTAs leaves fp32
+//                          shared-memory window (all shapes but e4m3 head_dim
+//                          128) and TMA-loads the K/V tiles it consumes from
+//                          this GPU's memory into its own shared memory.  A tile cut between CTAs leaves fp32
 //                          partials + LSE.
 //                          Warp roles: warps 4 and 6 issue TMA loads (K ring,
 //                          V ring; warp 7 shares the K boxes of tiles of small

@@ -98,8 +98,10 @@ dg_status_t dg_attn_forward(const void* q, const void* k, const void* v,
 /* Same as dg_attn_forward, and additionally records the caller's CUDA events
  * (cudaEvent_t, either may be NULL) on `stream` immediately before and after
  * the launch of the main attention kernel, so a caller can time that kernel
- * alone (the work-list build before it and the split-KV merge after it fall
- * outside the two events). */
+ * alone (the split-KV merge after it, and the work-list grid before it where
+ * there is one, fall outside the two events; batches of at most 256 query
+ * tiles with contiguous K/V have no work-list grid, the attention kernel's
+ * CTAs build the list themselves, inside the events). */
 dg_status_t dg_attn_forward_profiled(const void* q, const void* k, const void* v,
                                      const int32_t* cu_q, const int32_t* ctx_len,
                                      const uint8_t* mode, int32_t num_seqs, int32_t total_q,
