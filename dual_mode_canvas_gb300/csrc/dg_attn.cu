@@ -351,13 +351,21 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   const void* kmap = pg ? pg->k_cache : k;
   const void* vmap = pg ? pg->v_cache : v;
   const int map_rows = pg ? (pg->num_pages << pg->page_shift) : total_kv;
-  // V pages of exactly one MMA K step, and head_dim over several 128-byte
-  // blocks: one box per page (DG_ATTN_V_PAGE_BOX=0 keeps a box per block)
+  // V pages of one MMA K step or half of one, and head_dim over several
+  // 128-byte blocks: one box per page (DG_ATTN_V_PAGE_BOX=0 keeps a box per
+  // block)
   const int kstep = f8 ? 32 : 16;
   const int nkb = head_dim * (f8 ? 1 : 2) / 128;
   const char* vpb_env = std::getenv("DG_ATTN_V_PAGE_BOX");
-  const bool v_page_box = pg && box == kstep && box < BN && nkb > 1 && !(vpb_env && std::strcmp(vpb_env, "0") == 0);
-  if (encode_map(&mk, kmap, map_rows, num_kv_heads, head_dim, 1, box, f8) != DG_OK ||
+  const bool v_page_box = pg && (box == kstep || 2 * box == kstep) && box < BN && nkb > 1 &&
+                          !(vpb_env && std::strcmp(vpb_env, "0") == 0);
+  // K pages of 8 rows: one box per page as well (DG_ATTN_K_PAGE_BOX=0 keeps a
+  // box per block)
+  const char* kpb_env = std::getenv("DG_ATTN_K_PAGE_BOX");
+  const bool k_page_box = pg && !f8 && box == 8 && box < BN && nkb > 1 &&
+                          !(kpb_env && std::strcmp(kpb_env, "0") == 0);
+  if ((k_page_box ? encode_page_map(&mk, kmap, map_rows, num_kv_heads, head_dim, box, f8)
+                  : encode_map(&mk, kmap, map_rows, num_kv_heads, head_dim, 1, box, f8)) != DG_OK ||
       (v_page_box ? encode_page_map(&mv, vmap, map_rows, num_kv_heads, head_dim, box, f8)
                   : encode_map(&mv, vmap, map_rows, num_kv_heads, head_dim, 1, box, f8)) != DG_OK)
     return DG_ERR_INVALID_ARG;
@@ -383,9 +391,11 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   p.page_shift = pg ? pg->page_shift : 0;
   p.page_box = box;
   p.v_page_box = v_page_box ? 1 : 0;
+  p.k_page_box = k_page_box ? 1 : 0;
   // a K tile of 8 or more boxes: two warps issue them (DG_ATTN_K_SPLIT=0: one)
   const char* ks_env = std::getenv("DG_ATTN_K_SPLIT");
-  p.k_split = ((BN / box) * nkb >= 8 && !(ks_env && std::strcmp(ks_env, "0") == 0)) ? 1 : 0;
+  const int k_boxes = k_page_box ? BN / box : (BN / box) * nkb;
+  p.k_split = (k_boxes >= 8 && !(ks_env && std::strcmp(ks_env, "0") == 0)) ? 1 : 0;
   // segment weight in KV-tile units: a segment (Q load, pipeline fill,
   // epilogue) costs about the same time at every head_dim, a 64-key tile of
   // head_dim 256 less than a 128-key one.  Measured optima: 18 for 64-key

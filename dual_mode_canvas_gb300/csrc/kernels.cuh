@@ -30,7 +30,7 @@
 // 1.. of the launch) and checks every page-table entry the attention will
 // read; the loaders look up each tile's pages and load them in boxes of
 // min(P, BN) rows, one box per lane of the loader warp (V pages of one MMA K
-// step in one box per page).
+// step or half of one, and K pages of 8 rows, in one box per page).
 //
 // Rules (DiffusionGemma, agentlenshq page, "dual-mode operation", "dynamic
 // per-sequence causal attention", "symmetric sliding-window attention"): a
@@ -148,12 +148,18 @@ struct FwdParams {
   int page_shift, page_box;
   // 1: the V tensor map is 4-D ({128-byte block, head, row, column block})
   // and one box brings a whole page (page_box rows, every column block of
-  // head_dim): a page of one MMA K step (16 bf16 / 32 e4m3 rows) lands as
-  // [column block][row][128 bytes], which P.V reads with the column-block
-  // stride of one page.  Cuts a 16-row-page V tile from NKB boxes per page to
-  // one.  (K cannot: QK^T's B operand needs every key row of a column block at
-  // one stride.)
+  // head_dim): a page of one MMA K step (16 bf16 / 32 e4m3 rows), or of half
+  // of one (8 bf16 rows), lands as [column block][row][128 bytes], which P.V
+  // reads with the column-block stride of one page (and, for 8-row pages, the
+  // next 8 rows one page further on).  Cuts a small-page V tile from NKB
+  // boxes per page to one.
   int v_page_box;
+  // 1: the same whole-page boxes for K, with 8-row pages only: a page is then
+  // one 8-row swizzle group of every column block, so QK^T's B operand finds
+  // consecutive 8-row groups of a column block one page (NKB * 1024 bytes)
+  // apart.  (Larger pages hold several groups of a column block together, at
+  // another stride than the next page's.)
+  int k_page_box;
   // 1: two warps issue a K tile's TMA boxes, half each (each registers its
   // half of the bytes on K_FULL, which then counts two arrivals).  A K tile of
   // small pages is 16 or more boxes, and one warp issuing them one after the
@@ -1166,7 +1172,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     // (at most 32: a box holds at least 8 rows, BN * NKB <= 256)
     const int box_rows = paged ? p.page_box : BN;
     const int nbr = BN / box_rows;
-    const bool page_box = !is_k && p.v_page_box;  // one box per page, every column block
+    const bool page_box = is_k ? p.k_page_box : p.v_page_box;  // one box per page, every column block
     const int box_i = lane * nkw + kw;              // boxes interleaved over the warps
     const bool has_box = box_i < (page_box ? nbr : nbr * Cf::NKB);
     const int br = page_box ? box_i : box_i % nbr, bk = page_box ? 0 : box_i / nbr;
@@ -1285,9 +1291,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       bool ok = true;
       bool k_ready = false;  // the next QK's K stage was seen full by the last probe
       // V tile layout: [column block][BN rows][128 B] (column blocks BN * 128
-      // bytes apart, a K step KSTEP rows further on), or with whole-page
-      // boxes [page][column block][KSTEP rows][128 B] (a page per K step)
-      const uint32_t pv_lbo = p.v_page_box ? E::KSTEP * 128 : BN * 128;
+      // bytes apart, 8-row groups 1024 apart, a K step KSTEP rows further on),
+      // or with whole-page boxes [page][column block][page rows][128 B]:
+      // column blocks page_box * 128 bytes apart, 8-row groups 1024 apart in a
+      // page of one K step and one page (NKB * 1024) apart with 8-row pages, a
+      // K step NKB * KSTEP * 128 bytes further on either way
+      const uint32_t pv_lbo = p.v_page_box ? p.page_box * 128 : BN * 128;
+      const uint32_t pv_sbo = (!F8 && p.v_page_box && p.page_box == 8) ? Cf::NKB * 1024 : 1024;
       const uint32_t pv_step_bytes = p.v_page_box ? Cf::NKB * E::KSTEP * 128 : E::KSTEP * 128;
       Seg sg;
       while (ok && it.next(sg)) {
@@ -1311,7 +1321,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             // advances 8 TMEM columns, B 32 bytes within the swizzle atom
 #pragma unroll
             for (int kb = 0; kb < Cf::NKB; ++kb) {
-              const uint64_t b = smem_desc_sw128(k_base + kb * (BN * 128), 16, 1024);
+              // column block kb: BN rows of 128 bytes, or with 8-row page
+              // boxes 8 rows per page, pages NKB * 1024 bytes apart
+              const uint64_t b = (!F8 && p.k_page_box)
+                                     ? smem_desc_sw128(k_base + kb * 1024, 16, Cf::NKB * 1024)
+                                     : smem_desc_sw128(k_base + kb * (BN * 128), 16, 1024);
               if constexpr (QS) {
                 // A from the query tile in shared memory: 32 bytes per K step
                 const uint64_t a = smem_desc_sw128(sQ + kb * (kRows * 128), 16, 1024);
@@ -1347,7 +1361,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             static_assert(kPvSteps % kPvBatch == 0, "P.V steps in batches of 2 or 4");
 #pragma unroll
             for (int kb = 0; kb < kPvSteps / kPvBatch; ++kb) {
-              const uint64_t b = smem_desc_sw128(v_base + kb * kPvBatch * pv_step_bytes, pv_lbo, 1024);
+              const uint64_t b = smem_desc_sw128(v_base + kb * kPvBatch * pv_step_bytes, pv_lbo, pv_sbo);
               umma_ts_batch_warp<F8, kPvBatch>(tmem + Cf::TM_O, p_tm + kb * kPvBatch * 8, b, idesc_pv,
                                                (first && kb == 0) ? 0u : 1u, 8u,
                                                static_cast<uint64_t>(pv_step_bytes / 16));

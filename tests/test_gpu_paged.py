@@ -125,15 +125,18 @@ def test_paged_equals_contiguous_bit_for_bit(P, D):
     assert torch.equal(lse_p, lse_c)
 
 
-@pytest.mark.parametrize("knob", ["DG_ATTN_V_PAGE_BOX", "DG_ATTN_K_SPLIT"])
+@pytest.mark.parametrize("knob", ["DG_ATTN_V_PAGE_BOX", "DG_ATTN_K_PAGE_BOX", "DG_ATTN_K_SPLIT"])
 @pytest.mark.parametrize("D", [128, 256])
-def test_box_layouts_give_the_same_bits(D, knob, monkeypatch):
-    """16-row pages: the default loads (V as one box per page, a K tile's boxes
-    issued by two warps) and the plain ones (a V box per page and 128-byte
-    column block; one K warp) give the same bits."""
+@pytest.mark.parametrize("P", [8, 16])
+def test_box_layouts_give_the_same_bits(P, D, knob, monkeypatch):
+    """8- and 16-row pages: the default loads (V as one box per page, read
+    with a page stride between 8-row groups when a page is half a K step; K as
+    one box per 8-row page, its 8-row groups a page apart; a K tile's boxes
+    issued by two warps) and the plain ones (a box per page and 128-byte column
+    block; one K warp) give the same bits."""
     Hq, Hkv = (8, 4) if D == 128 else (16, 2)
     wl = wls.Workload("vbox", ((700, 256, 1), (0, 190, 0)), Hq, Hkv, D, -1, 78)
-    b = wls.make_paged_batch(wl, 16, device="cuda")
+    b = wls.make_paged_batch(wl, P, device="cuda")
     d = to_dev(b)
     out_a, lse_a = run_paged(d, -1, wl.scale, append=False)
     monkeypatch.setenv(knob, "0")
