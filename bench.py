@@ -477,7 +477,8 @@ def run_gpu(args):
         "algorithmic_gflop_per_step": round(flops / 1e9, 3),
         "algorithmic_mb_per_step": round(nbytes / 1e6, 3),
         "wall_s_timed_region": round(t_wall, 3),
-        "gpu_launches": 3 * args.steps * world,
+        "gpu_launches": binding.launches_per_call(len(wl.seqs), wl.total_q, wl.num_q_heads, wl.num_kv_heads,
+                                                  wl.head_dim, paged, fp8) * args.steps * world,
         "roofline": roof,
         "clocks": clk,
     }
@@ -492,7 +493,8 @@ def run_gpu(args):
             "algorithmic_gflop_per_step": round(m4["flops"] / 1e9, 3),
             "algorithmic_mb_per_step": round(m4["nbytes"] / 1e6, 3),
             "l2": "flushed before every step (256 MiB write)",
-            "gpu_launches": 3 * args.steps * world,
+            "gpu_launches": binding.launches_per_call(len(w4.seqs), w4.total_q, w4.num_q_heads,
+                                                      w4.num_kv_heads, w4.head_dim) * args.steps * world,
             "roofline": attention_roofline(m4, peaks, peaks_src, "maxmix_full"),
             "clocks": m4["clocks"]}}
     if e2e is not None:

@@ -30,7 +30,7 @@ DG_MODE_BIDIRECTIONAL = 1
 # capacity of dg_attn_forward_noalloc's static scratch (DG_ATTN_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 48 << 20
 
-EXPORTED = ("dg_attn_workspace_size", "dg_attn_forward", "dg_attn_forward_profiled",
+EXPORTED = ("dg_attn_workspace_size", "dg_attn_launches_per_call", "dg_attn_forward", "dg_attn_forward_profiled",
             "dg_attn_forward_noalloc", "dg_attn_forward_paged", "dg_attn_forward_paged_profiled",
             "dg_attn_forward_fp8", "dg_attn_forward_fp8_profiled",
             "dg_selfcond_workspace_size", "dg_selfcond_forward", "dg_selfcond_forward_profiled",
@@ -67,6 +67,8 @@ def load_library(debug: bool | None = None):
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     lib.dg_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     lib.dg_attn_workspace_size.restype = sz
+    lib.dg_attn_launches_per_call.argtypes = [i32] * 7
+    lib.dg_attn_launches_per_call.restype = i32
     lib.dg_attn_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                     ctypes.c_float, vp, vp, vp, sz, vp]
     lib.dg_attn_forward.restype = ctypes.c_int
@@ -139,6 +141,13 @@ def workspace_size(num_seqs: int, total_q: int, num_q_heads: int, num_kv_heads: 
                    head_dim: int) -> int:
     return int(load_library().dg_attn_workspace_size(num_seqs, total_q, num_q_heads, num_kv_heads,
                                                      head_dim))
+
+
+def launches_per_call(num_seqs: int, total_q: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                      paged: bool = False, e4m3: bool = False) -> int:
+    """Kernels one forward call with these sizes launches (2 or 3)."""
+    return int(load_library().dg_attn_launches_per_call(num_seqs, total_q, num_q_heads, num_kv_heads,
+                                                        head_dim, int(paged), int(e4m3)))
 
 
 def _stream_handle(stream) -> int:

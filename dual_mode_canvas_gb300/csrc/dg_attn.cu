@@ -274,6 +274,26 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 using namespace dg;
 
+namespace {
+// The attention grid builds the work list itself (no work-list grid) for
+// contiguous K/V batches whose tile bound fits the per-CTA tables, but not in
+// the e4m3 head_dim-128 shape, whose kernel reads the work-list grid's tables
+// directly; DG_ATTN_FUSED_WL=0 keeps the separate grid everywhere.
+bool fused_work_list(bool paged, bool f8, int head_dim, const Layout& lay) {
+  const char* e = std::getenv("DG_ATTN_FUSED_WL");
+  return !paged && lay.local && !(f8 && head_dim == 128) && !(e && std::strcmp(e, "0") == 0);
+}
+}  // namespace
+
+extern "C" int32_t dg_attn_launches_per_call(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim, int32_t paged,
+                                             int32_t e4m3) {
+  if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim)) return 0;
+  // (the layout's tile bound does not depend on the SM count)
+  const Layout lay = make_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, 1);
+  return fused_work_list(paged != 0, e4m3 != 0, head_dim, lay) ? 2 : 3;
+}
+
 extern "C" size_t dg_attn_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
                                          int32_t num_kv_heads, int32_t head_dim) {
   if (!sizes_ok(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim)) return 0;
@@ -437,12 +457,7 @@ dg_status_t forward_impl(const void* q, const void* k, const void* v, const int3
   // Small batches with contiguous K/V have no work-list grid: every CTA of
   // the attention grid builds the list for itself (measured: the work-list
   // grid's launch and run cost a denoise step ~5 us on the critical path).
-  // DG_ATTN_FUSED_WL=0 keeps the separate grid.
-  const char* fwl_env = std::getenv("DG_ATTN_FUSED_WL");
-  // (not the e4m3 head_dim-128 shape, whose kernel reads the work-list grid's
-  // tables directly)
-  p.fused_wl = (!pg && lay.local && !(f8 && head_dim == 128) && !(fwl_env && std::strcmp(fwl_env, "0") == 0))
-                   ? 1 : 0;
+  p.fused_wl = fused_work_list(pg != nullptr, f8, head_dim, lay) ? 1 : 0;
   p.cu_q = cu_q;
   p.ctx_len = ctx_len;
   p.mode = mode;

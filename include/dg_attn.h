@@ -67,6 +67,17 @@ enum { DG_MODE_CAUSAL = 0, DG_MODE_BIDIRECTIONAL = 1 };
 size_t dg_attn_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
                               int32_t num_kv_heads, int32_t head_dim);
 
+/* Kernels one forward call with these sizes launches on its stream: 2 (the
+ * attention grid, which builds its work list itself, and the split-KV merge)
+ * for contiguous K/V batches of at most 256 query tiles (bounded from the
+ * sizes) other than e4m3 at head_dim 128, else 3 (a work-list grid first).
+ * paged / e4m3: nonzero for dg_attn_forward_paged / dg_attn_forward_fp8.
+ * Host only (no device needed); reads the same environment switch as the
+ * call.  Returns 0 when the sizes are invalid. */
+int32_t dg_attn_launches_per_call(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t paged,
+                                  int32_t e4m3);
+
 /* Dual-mode attention forward.
  *
  *   q          bf16 device [total_q, num_q_heads, head_dim], row-major, 16-byte aligned

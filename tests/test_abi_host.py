@@ -83,6 +83,22 @@ def test_host_checked_errors(lib, kw, code):
     assert _fwd(lib, **kw) == code
 
 
+def test_launches_per_call(lib, monkeypatch):
+    """The host-side rule for the launch chain: small contiguous batches have
+    no work-list grid (2 kernels), a batch past the per-CTA table bound, a
+    paged cache and the e4m3 head_dim-128 shape have one (3)."""
+    lp = binding.launches_per_call
+    assert lp(1, 256, 32, 4, 256) == 2                      # denoise loop: 4 x (16 + 1) tile bound
+    assert lp(4, 1024, 16, 8, 128) == 2                     # max mix: 160
+    assert lp(4, 2024, 16, 8, 128) == 3                     # mixed batch: 288 > 256
+    assert lp(1, 256, 32, 4, 256, paged=True) == 3          # the work-list grid appends the new rows
+    assert lp(4, 1024, 16, 8, 128, e4m3=True) == 3
+    assert lp(1, 256, 32, 4, 256, e4m3=True) == 2
+    assert lp(1, 256, 32, 5, 256) == 0                      # Hq % Hkv != 0
+    monkeypatch.setenv("DG_ATTN_FUSED_WL", "0")
+    assert lp(1, 256, 32, 4, 256) == 3
+
+
 def test_empty_batch_is_a_no_op(lib):
     assert _fwd(lib, B=0, total_q=0) == binding.DG_OK
     assert _fwd(lib, total_q=0) == binding.DG_OK
